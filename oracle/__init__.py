@@ -1,0 +1,45 @@
+"""CPU FP64 oracle for exact softmax self-attention.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path may import this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` use it. The CUDA path shares no code
+with it (no kernels, headers, helpers, constants or pre/post-processing).
+
+Modules
+-------
+``dense``        the plain definition of the result: O = softmax(scale*Q K^T +
+                 mask) V and the per-row logsumexp, computed densely in float64
+                 per (batch, head) or per packed sequence.
+``online_state`` the mergeable (running max m, rescaled exp-sum l, numerator
+                 acc) state with its explicit empty identity, the algebra the
+                 streaming method is built on.
+
+Sources (web pages, cited by title and section):
+  * "Intermediate and advanced extension" (triton-cuda-lab), workshop table row
+    "Streaming attention" and "Logic review before implementation".
+  * "Intermediate and advanced workshop validation" (triton-cuda-lab),
+    "Correctness and review".
+  * "Attention algorithms and data movement" (study.greatitself.com), lessons
+    01 (merging normalised attention), 04 (packed causal eligibility) and 05
+    (GQA head mapping).
+
+Parity status: every function here is pinned by CPU tests in
+``tests/test_oracle.py`` against closed forms, a hand-worked example, library
+routines (PyTorch's CPU scaled_dot_product_attention, SciPy's logsumexp),
+invariants and brute force; none is "parity unpinned".
+"""
+
+from .dense import attention_dense, attention_varlen, attention_rows, attention_varlen_rows
+from .online_state import State, empty_state, state_of_block, merge, finalize
+
+__all__ = [
+    "attention_dense",
+    "attention_varlen",
+    "attention_rows",
+    "attention_varlen_rows",
+    "State",
+    "empty_state",
+    "state_of_block",
+    "merge",
+    "finalize",
+]

@@ -1,0 +1,42 @@
+"""CPU checks of the seeded workload generators (shapes, seeds, lengths)."""
+
+import torch
+
+from exact_tiled_attention_19_gb300 import workloads as W
+
+
+def test_varlen_lengths_seed7():
+    assert W.varlen_lengths_from_seed(7) == W.VARLEN_LENGTHS_SEED7
+    assert sum(W.VARLEN_LENGTHS_SEED7) == 124825 and max(W.VARLEN_LENGTHS_SEED7) == 14891
+
+
+def test_cu_seqlens():
+    cu = W.cu_seqlens_of([3, 0, 5])
+    assert cu.tolist() == [0, 3, 3, 8] and cu.dtype == torch.int32
+
+
+def test_small_workload_shapes_and_determinism():
+    a = W.make_inputs("c1")
+    b = W.make_inputs("c1")
+    assert a["q"].shape == (1, 1, 129, 32) and a["q"].dtype == torch.float16
+    assert torch.equal(a["q"], b["q"]) and torch.equal(a["v"], b["v"])
+    big = W.make_inputs("c2_large_logit")
+    base = W.make_inputs("c2_causal")
+    assert torch.equal(big["k"], base["k"])
+    assert float(big["q"].float().abs().max()) > 20 * float(base["q"].float().abs().max()) * 0.9
+
+
+def test_transposed_layout_is_same_logical_values():
+    w = W.Workload("t", "t", 2, 3, 3, 17, 32, torch.bfloat16, True)
+    wt = W.Workload("t", "t", 2, 3, 3, 17, 32, torch.bfloat16, True, layout="bnhd")
+    a, b = W.make_inputs(w), W.make_inputs(wt)
+    assert torch.equal(a["q"], b["q"])
+    assert b["q"].stride() == (17 * 3 * 32, 32, 3 * 32, 1)
+
+
+def test_flop_and_byte_conventions():
+    c5 = W.WORKLOADS["c5"]
+    assert abs(c5.flops_convention() - 5.507e12) / 5.507e12 < 1e-3
+    c3 = W.WORKLOADS["c3"]
+    assert c3.flops_convention() == 4 * 4096 ** 2 * 128 * 64 / 2
+    assert c3.io_bytes() == 4 * 4 * 16 * 4096 * 128 * 2 + 4 * 16 * 4096 * 4
