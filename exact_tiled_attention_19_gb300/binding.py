@@ -1,0 +1,201 @@
+"""ctypes binding of the C ABI in ``include/etattn.h``.
+
+The functions ``attn_fwd``, ``attn_fwd_varlen``, ``etattn_status_string``,
+``etattn_last_cuda_error``, ``etattn_read_device_status`` and
+``etattn_version`` have the C names and arguments (pointers as ints).  The
+helpers ``attention`` and ``attention_varlen`` marshal torch CUDA tensors
+(output allocation, strides, the current stream) and call them; every step of
+the computation runs in the library's kernels.  There is no fallback: if the
+library is missing or cannot be loaded, an error is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libetattn.so")
+
+ETATTN_F16 = 0
+ETATTN_BF16 = 1
+STATUS_NAMES = {
+    0: "ETATTN_OK", 1: "ETATTN_ERR_NULL_PTR", 2: "ETATTN_ERR_BAD_DTYPE", 3: "ETATTN_ERR_BAD_SHAPE",
+    4: "ETATTN_ERR_BAD_HEADS", 5: "ETATTN_ERR_BAD_STRIDE", 6: "ETATTN_ERR_BAD_ALIGN", 7: "ETATTN_ERR_ALIAS",
+    8: "ETATTN_ERR_BAD_SCALE", 9: "ETATTN_ERR_BAD_SEQLENS", 10: "ETATTN_ERR_LAUNCH", 11: "ETATTN_ERR_DEVICE",
+    12: "ETATTN_ERR_NO_DEVICE",
+}
+
+
+class EtattnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = f"{where}: {STATUS_NAMES.get(code, code)} ({etattn_status_string(code)})"
+        if code == 10:
+            msg += f"; cudaError={etattn_last_cuda_error()}"
+        super().__init__(msg)
+
+
+_lib = None
+_lock = threading.Lock()
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+
+
+def load_library(path: str | None = None):
+    """Load libetattn.so (building it first when it is absent and nvcc is
+    available).  Raises OSError / RuntimeError when it cannot be loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            from . import build_lib
+            path = build_lib.build()
+        lib = ctypes.CDLL(path)
+        lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _i64p, _int,
+                                 ctypes.c_float, _vp]
+        lib.attn_fwd.restype = _int
+        lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
+                                        _int, _i64p, _int, ctypes.c_float, _vp]
+        lib.attn_fwd_varlen.restype = _int
+        lib.etattn_status_string.argtypes = [_int]
+        lib.etattn_status_string.restype = ctypes.c_char_p
+        lib.etattn_last_cuda_error.argtypes = []
+        lib.etattn_last_cuda_error.restype = _int
+        lib.etattn_read_device_status.argtypes = [ctypes.POINTER(_int), _int, _vp]
+        lib.etattn_read_device_status.restype = _int
+        lib.etattn_version.argtypes = []
+        lib.etattn_version.restype = _int
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- raw C entry points
+
+def _strides_arg(strides):
+    arr = (ctypes.c_int64 * len(strides))(*[int(s) for s in strides])
+    return arr
+
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, dtype, strides, causal, scale, stream):
+    """C ``attn_fwd``: pointers as ints (0 for NULL), ``strides`` 16 ints."""
+    lib = load_library()
+    return lib.attn_fwd(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, N, D, dtype,
+                        _strides_arg(strides), causal, scale, stream or None)
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, cu_seqlens_host, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D,
+                    dtype, strides, causal, scale, stream):
+    """C ``attn_fwd_varlen``: pointers as ints; ``cu_seqlens_host`` is an int
+    address of a host int32 array or 0; ``strides`` 12 ints."""
+    lib = load_library()
+    return lib.attn_fwd_varlen(q or None, k or None, v or None, o or None, lse or None, cu_seqlens or None,
+                               cu_seqlens_host or None, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D, dtype,
+                               _strides_arg(strides), causal, scale, stream or None)
+
+
+def etattn_status_string(code: int) -> str:
+    return load_library().etattn_status_string(code).decode()
+
+
+def etattn_last_cuda_error() -> int:
+    return load_library().etattn_last_cuda_error()
+
+
+def etattn_read_device_status(clear: bool = True, stream: int = 0) -> int:
+    out = _int(0)
+    rc = load_library().etattn_read_device_status(ctypes.byref(out), 1 if clear else 0, stream or None)
+    if rc != 0:
+        raise EtattnError(rc, "etattn_read_device_status")
+    return out.value
+
+
+def etattn_version() -> int:
+    return load_library().etattn_version()
+
+
+# ---------------------------------------------------------------- torch marshalling
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return ETATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ETATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def attention(q, k, v, *, causal: bool = True, scale: float | None = None, out=None, lse=None,
+              return_lse: bool = True, stream=None):
+    """Batched (GQA-capable) attention on CUDA tensors.
+
+    q: [B, Hq, N, D]; k, v: [B, Hkv, N, D] (any strides with d contiguous,
+    e.g. a [B, N, H, D] buffer viewed through permute).  Returns (o, lse) with
+    o a new [B, Hq, N, D] tensor (or ``out``) and lse a new [B, Hq, N] FP32
+    tensor (or ``lse``; None when ``return_lse`` is False)."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, N, D), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, N) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, N] tensor")
+    strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
+    with torch.cuda.device(q.device):
+        rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      lse.data_ptr() if lse is not None else 0, B, Hq, Hkv, N, D, _dtype_code(q), strides,
+                      1 if causal else 0, float(scale), _stream_handle(stream))
+    if rc != 0:
+        raise EtattnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = True, scale: float | None = None,
+                     cu_seqlens_host=None, out=None, lse=None, return_lse: bool = True, stream=None):
+    """Packed variable-length attention on CUDA tensors.
+
+    q: [T, Hq, D]; k, v: [T, Hkv, D]; cu_seqlens: int32 CUDA tensor [S+1].
+    ``cu_seqlens_host`` (optional int32 CPU tensor) is validated before launch.
+    Returns (o [T, Hq, D], lse [Hq, T] FP32 or None)."""
+    import torch
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    S = cu_seqlens.shape[0] - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+        raise TypeError("cu_seqlens must be an int32 CUDA tensor")
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    host_ptr = 0
+    if cu_seqlens_host is not None:
+        cu_seqlens_host = cu_seqlens_host.to(torch.int32).contiguous()
+        host_ptr = cu_seqlens_host.data_ptr()
+    strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
+    with torch.cuda.device(q.device):
+        rc = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr() if lse is not None else 0, cu_seqlens.data_ptr(), host_ptr, S,
+                             int(max_seqlen), T, Hq, Hkv, D, _dtype_code(q), strides, 1 if causal else 0,
+                             float(scale), _stream_handle(stream))
+    if rc != 0:
+        raise EtattnError(rc, "attn_fwd_varlen")
+    return out, lse

@@ -1,0 +1,365 @@
+// Host side of the C ABI declared in etattn.h: argument validation (all of it
+// before any CUDA call), TMA tensor-map encoding and kernel launch.
+//
+// The validation contract follows "Intermediate and advanced extension",
+// "Code review and execution gates": shapes, layouts, dtypes, index spans and
+// launch knobs are checked before a kernel is invoked, inputs are read-only
+// and outputs are separate allocations.
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "attn_fwd_kernel.cuh"
+#include "etattn.h"
+#include "launchers.h"
+
+namespace etattn {
+
+// Device status word shared by every launch on a device (0 = ok).
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxTokens = 65535 * 128;  // grid.y bound on query tiles
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return ETATTN_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------- validation helpers
+struct View {         // a strided tensor of rank <= 4, sizes and strides in elements
+  const void* ptr;
+  int rank;
+  int64_t size[4];
+  int64_t stride[4];
+};
+
+// Byte span [lo, hi) touched by a view (hi == lo when it is empty).
+void span_of(const View& v, size_t esz, uintptr_t* lo, uintptr_t* hi) {
+  *lo = reinterpret_cast<uintptr_t>(v.ptr);
+  uint64_t last = 0;
+  for (int i = 0; i < v.rank; ++i) {
+    if (v.size[i] == 0) {
+      *hi = *lo;
+      return;
+    }
+    last += (uint64_t)(v.size[i] - 1) * (uint64_t)v.stride[i];
+  }
+  *hi = *lo + (last + 1) * esz;
+}
+
+bool overlaps(const View& a, size_t ea, const View& b, size_t eb) {
+  uintptr_t alo, ahi, blo, bhi;
+  span_of(a, ea, &alo, &ahi);
+  span_of(b, eb, &blo, &bhi);
+  if (alo == ahi || blo == bhi) return false;
+  return alo < bhi && blo < ahi;
+}
+
+// d-stride 1; every other stride of an extent > 1 positive and a multiple of 16 bytes.
+bool strides_ok(const View& v, size_t esz) {
+  if (v.stride[v.rank - 1] != 1) return false;
+  for (int i = 0; i < v.rank - 1; ++i) {
+    if (v.size[i] <= 1) continue;
+    if (v.stride[i] <= 0) return false;
+    if (((uint64_t)v.stride[i] * esz) % 16 != 0) return false;
+    if ((uint64_t)v.stride[i] * esz >= (1ull << 40)) return false;
+  }
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device / driver plumbing
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 ok, 2 unsupported
+  int* status_word = nullptr;
+};
+DeviceInfo g_devices[64];
+std::mutex g_device_mu;
+
+// Current device, checked to be sm_103, with its status-word address.
+int current_device(int* dev_out, int** status_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return ETATTN_ERR_NO_DEVICE;
+  }
+  DeviceInfo& d = g_devices[dev];
+  if (d.state.load(std::memory_order_acquire) == 0) {
+    std::lock_guard<std::mutex> lk(g_device_mu);
+    if (d.state.load() == 0) {
+      int major = 0, minor = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return ETATTN_ERR_NO_DEVICE;
+      }
+      if (major != 10 || minor != 3) {
+        d.state.store(2);
+      } else {
+        void* sym = nullptr;
+        cudaError_t se = cudaGetSymbolAddress(&sym, g_status_word);
+        if (se != cudaSuccess) return fail_cuda(se);
+        d.status_word = static_cast<int*>(sym);
+        d.state.store(1, std::memory_order_release);
+      }
+    }
+  }
+  if (d.state.load() != 1) return ETATTN_ERR_NO_DEVICE;
+  *dev_out = dev;
+  *status_out = d.status_word;
+  return ETATTN_OK;
+}
+
+// 4-D tensor map over (d, token, head, batch) with a box of one 128-row tile
+// of SW elements along d.  If the token stride exceeds the head stride the
+// two middle axes are exchanged so that strides grow outward; *swapped says so.
+int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_tokens, int64_t n_heads,
+               int64_t n_batch, int64_t s_tok, int64_t s_head, int64_t s_batch, bool* swapped) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return fail_cuda(cudaErrorNotSupported);
+  const uint64_t esz = 2;
+  const int sw_elems = D >= 64 ? 64 : 32;
+  // Strides of extent-1 axes are never used; give them a harmless value.
+  uint64_t reach = 16;
+  if (n_tokens > 1) reach = std::max<uint64_t>(reach, (uint64_t)s_tok * esz * (uint64_t)n_tokens);
+  if (n_heads > 1) reach = std::max<uint64_t>(reach, (uint64_t)s_head * esz * (uint64_t)n_heads);
+  if (n_batch > 1) reach = std::max<uint64_t>(reach, (uint64_t)s_batch * esz * (uint64_t)n_batch);
+  reach = (reach + 15) & ~uint64_t(15);
+  const uint64_t bt = n_tokens > 1 ? (uint64_t)s_tok * esz : reach;
+  const uint64_t bh = n_heads > 1 ? (uint64_t)s_head * esz : reach;
+  const uint64_t bb = n_batch > 1 ? (uint64_t)s_batch * esz : reach;
+  const bool sw = n_tokens > 1 && n_heads > 1 && bt > bh;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)(sw ? n_heads : n_tokens), (cuuint64_t)(sw ? n_tokens : n_heads),
+                        (cuuint64_t)n_batch};
+  cuuint64_t strides[3] = {sw ? bh : bt, sw ? bt : bh, bb};
+  cuuint32_t box[4] = {(cuuint32_t)sw_elems, sw ? 1u : 128u, sw ? 128u : 1u, 1u};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, dtype == ETATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                   const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+  *swapped = sw;
+  return ETATTN_OK;
+}
+
+cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                   const FwdParams& p, unsigned gx, unsigned gy, cudaStream_t s) {
+  const bool bf = dtype == ETATTN_BF16;
+  switch (D) {
+    case 32: return bf ? launch_fwd_d32_1(q, k, v, p, gx, gy, s) : launch_fwd_d32_0(q, k, v, p, gx, gy, s);
+    case 64: return bf ? launch_fwd_d64_1(q, k, v, p, gx, gy, s) : launch_fwd_d64_0(q, k, v, p, gx, gy, s);
+    default: return bf ? launch_fwd_d128_1(q, k, v, p, gx, gy, s) : launch_fwd_d128_0(q, k, v, p, gx, gy, s);
+  }
+}
+
+bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 128; }
+
+}  // namespace
+}  // namespace etattn
+
+using namespace etattn;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
+  if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
+  if (B < 0 || Hq < 0 || N < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
+  if (N > kMaxTokens || (int64_t)B * Hq > INT_MAX) return ETATTN_ERR_BAD_SHAPE;
+  if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
+  if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
+  if (B == 0 || Hq == 0 || N == 0) return ETATTN_OK;  // empty output: nothing to do
+  if (!q || !k || !v || !o) return ETATTN_ERR_NULL_PTR;
+
+  const View vq{q, 4, {B, Hq, N, D}, {strides[0], strides[1], strides[2], strides[3]}};
+  const View vk{k, 4, {B, Hkv, N, D}, {strides[4], strides[5], strides[6], strides[7]}};
+  const View vv{v, 4, {B, Hkv, N, D}, {strides[8], strides[9], strides[10], strides[11]}};
+  const View vo{o, 4, {B, Hq, N, D}, {strides[12], strides[13], strides[14], strides[15]}};
+  const View vl{lse, 3, {B, Hq, N, 0}, {(int64_t)Hq * N, N, 1, 0}};
+  for (const View* t : {&vq, &vk, &vv, &vo})
+    if (!strides_ok(*t, 2)) return ETATTN_ERR_BAD_STRIDE;
+  for (const void* ptr : {q, k, v, (const void*)o})
+    if (!aligned16(ptr)) return ETATTN_ERR_BAD_ALIGN;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ETATTN_ERR_BAD_ALIGN;
+  for (const View* t : {&vq, &vk, &vv})
+    if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
+  if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
+
+  int dev = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status)) return rc;
+
+  CUtensorMap mq, mk, mv;
+  bool swq = false, swk = false, swv = false;
+  if (int rc = encode_map(&mq, dtype, q, D, N, Hq, B, strides[2], strides[1], strides[0], &swq)) return rc;
+  if (int rc = encode_map(&mk, dtype, k, D, N, Hkv, B, strides[6], strides[5], strides[4], &swk)) return rc;
+  if (int rc = encode_map(&mv, dtype, v, D, N, Hkv, B, strides[10], strides[9], strides[8], &swv)) return rc;
+
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_sb = strides[12];
+  p.o_sh = strides[13];
+  p.o_sn = strides[14];
+  p.lse_sb = (int64_t)Hq * N;
+  p.lse_sh = N;
+  p.cu_seqlens = nullptr;
+  p.N = N;
+  p.total_tokens = N;
+  p.max_seqlen = N;
+  p.Hq = Hq;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
+  const unsigned gx = (unsigned)(B * Hq), gy = (unsigned)((N + 127) / 128);
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ETATTN_OK;
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                    const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
+                    int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
+  if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
+  if (num_seqs < 0 || max_seqlen < 0 || total_tokens < 0 || Hq < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
+  if (max_seqlen > kMaxTokens || (int64_t)num_seqs * Hq > INT_MAX) return ETATTN_ERR_BAD_SHAPE;
+  if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
+  if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
+  if (cu_seqlens_host) {
+    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens) return ETATTN_ERR_BAD_SEQLENS;
+    for (int s = 0; s < num_seqs; ++s) {
+      const int64_t len = (int64_t)cu_seqlens_host[s + 1] - cu_seqlens_host[s];
+      if (len < 0 || len > max_seqlen) return ETATTN_ERR_BAD_SEQLENS;
+    }
+  }
+  if (num_seqs == 0 || Hq == 0 || total_tokens == 0 || max_seqlen == 0) return ETATTN_OK;
+  if (!q || !k || !v || !o || !cu_seqlens) return ETATTN_ERR_NULL_PTR;
+
+  const int T = total_tokens;
+  const View vq{q, 3, {T, Hq, D, 0}, {strides[0], strides[1], strides[2], 0}};
+  const View vk{k, 3, {T, Hkv, D, 0}, {strides[3], strides[4], strides[5], 0}};
+  const View vv{v, 3, {T, Hkv, D, 0}, {strides[6], strides[7], strides[8], 0}};
+  const View vo{o, 3, {T, Hq, D, 0}, {strides[9], strides[10], strides[11], 0}};
+  const View vl{lse, 2, {Hq, T, 0, 0}, {T, 1, 0, 0}};
+  for (const View* t : {&vq, &vk, &vv, &vo})
+    if (!strides_ok(*t, 2)) return ETATTN_ERR_BAD_STRIDE;
+  for (const void* ptr : {q, k, v, (const void*)o})
+    if (!aligned16(ptr)) return ETATTN_ERR_BAD_ALIGN;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ETATTN_ERR_BAD_ALIGN;
+  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return ETATTN_ERR_BAD_ALIGN;
+  for (const View* t : {&vq, &vk, &vv})
+    if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
+  if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
+
+  int dev = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status)) return rc;
+
+  CUtensorMap mq, mk, mv;
+  bool swq = false, swk = false, swv = false;
+  if (int rc = encode_map(&mq, dtype, q, D, T, Hq, 1, strides[0], strides[1], 0, &swq)) return rc;
+  if (int rc = encode_map(&mk, dtype, k, D, T, Hkv, 1, strides[3], strides[4], 0, &swk)) return rc;
+  if (int rc = encode_map(&mv, dtype, v, D, T, Hkv, 1, strides[6], strides[7], 0, &swv)) return rc;
+
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_sb = 0;
+  p.o_sh = strides[10];
+  p.o_sn = strides[9];
+  p.lse_sb = 0;
+  p.lse_sh = T;
+  p.cu_seqlens = cu_seqlens;
+  p.N = 0;
+  p.total_tokens = T;
+  p.max_seqlen = max_seqlen;
+  p.Hq = Hq;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
+  const unsigned gx = (unsigned)(num_seqs * Hq), gy = (unsigned)((max_seqlen + 127) / 128);
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ETATTN_OK;
+}
+
+const char* etattn_status_string(int code) {
+  switch (code) {
+    case ETATTN_OK: return "ok";
+    case ETATTN_ERR_NULL_PTR: return "a required pointer is NULL";
+    case ETATTN_ERR_BAD_DTYPE: return "unsupported dtype (expected F16 or BF16)";
+    case ETATTN_ERR_BAD_SHAPE: return "bad shape (negative size, head dim not 32/64/128, or beyond limits)";
+    case ETATTN_ERR_BAD_HEADS: return "bad head mapping (Hkv <= 0 or Hq not a multiple of Hkv)";
+    case ETATTN_ERR_BAD_STRIDE: return "bad stride (d-stride must be 1; others positive multiples of 16 bytes)";
+    case ETATTN_ERR_BAD_ALIGN: return "a base pointer is not 16-byte aligned";
+    case ETATTN_ERR_ALIAS: return "an output overlaps an input or the other output";
+    case ETATTN_ERR_BAD_SCALE: return "scale must be finite and > 0";
+    case ETATTN_ERR_BAD_SEQLENS: return "bad cu_seqlens (must rise from 0 to total_tokens, lengths <= max_seqlen)";
+    case ETATTN_ERR_LAUNCH: return "a CUDA runtime call failed";
+    case ETATTN_ERR_DEVICE: return "the device reported a failure (a bounded wait ran out)";
+    case ETATTN_ERR_NO_DEVICE: return "no sm_103 CUDA device is current";
+    default: return "unknown status";
+  }
+}
+
+int etattn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int etattn_read_device_status(int* out, int clear, void* stream) {
+  if (!out) return ETATTN_ERR_NULL_PTR;
+  int dev = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  int word = 0;
+  e = cudaMemcpy(&word, status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (clear && word != 0) {
+    e = cudaMemset(status, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  *out = word == kDevOk ? ETATTN_OK : word == kDevBadSeqlens ? ETATTN_ERR_BAD_SEQLENS : ETATTN_ERR_DEVICE;
+  return ETATTN_OK;
+}
+
+int etattn_version(void) { return 100; }
+
+}  // extern "C"

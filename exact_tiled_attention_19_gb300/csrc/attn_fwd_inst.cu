@@ -1,0 +1,43 @@
+// One (head dim, element type) instantiation of the forward kernel and its
+// launcher.  The build compiles this file once per variant with
+// -DETATTN_INST_D=<32|64|128> -DETATTN_INST_BF16=<0|1>, so the variants
+// compile in parallel.
+#include <atomic>
+#include <cuda_runtime.h>
+
+#include "attn_fwd_kernel.cuh"
+#include "launchers.h"
+
+#ifndef ETATTN_INST_D
+#error "ETATTN_INST_D must be defined"
+#endif
+#ifndef ETATTN_INST_BF16
+#error "ETATTN_INST_BF16 must be defined"
+#endif
+
+#define ETATTN_CAT2(a, b, c) a##b##_##c
+#define ETATTN_CAT(a, b, c) ETATTN_CAT2(a, b, c)
+#define ETATTN_LAUNCHER ETATTN_CAT(launch_fwd_d, ETATTN_INST_D, ETATTN_INST_BF16)
+
+namespace etattn {
+
+cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
+                            unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
+  using C = TileCfg<ETATTN_INST_D>;
+  auto kern = attn_fwd_kernel<ETATTN_INST_D, ETATTN_INST_BF16 != 0>;
+  // The dynamic shared-memory opt-in is per device; set it once per device.
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  kern<<<dim3(grid_x, grid_y, 1), C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace etattn

@@ -1,0 +1,131 @@
+/*
+ * etattn.h: C ABI of the exact streaming self-attention forward pass for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation ("Intermediate and advanced extension", workshop table row
+ * "Streaming attention" and "Logic review before implementation"):
+ *
+ *   O_i   = sum_{j in E(i)} exp(s_ij - M_i) v_j / sum_{j in E(i)} exp(s_ij - M_i)
+ *   lse_i = M_i + ln sum_{j in E(i)} exp(s_ij - M_i)        (natural log, FP32)
+ *   s_ij  = scale * <q_i, k_j>,   M_i = max_{j in E(i)} s_ij
+ *
+ * computed tile by tile with a running maximum and a rescaled exponential sum,
+ * rescaling both the numerator accumulator and the denominator whenever the
+ * maximum grows, without ever materialising the score matrix.  E(i) is every
+ * key, or under the causal mask the keys j <= i (the diagonal is included, so
+ * no causal row is empty).  Grouped-query attention ("Attention algorithms and
+ * data movement", lesson 05): query head h reads key/value head
+ * h / (Hq / Hkv).  Packed variable-length batches (same page, lesson 04):
+ * positions are logical positions inside each sequence and no key is eligible
+ * across sequences.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - q, k, v, o are DEVICE pointers to FP16 or BF16 data (all four the same
+ *    type, chosen by `dtype`); lse is a DEVICE pointer to FP32 or NULL (then
+ *    no logsumexp is written).  Strides are in ELEMENTS, not bytes.
+ *  - The caller owns every buffer.  Inputs are only read; o and lse are only
+ *    written (o and lse must not overlap q, k, v or each other).  The library
+ *    allocates no device memory per call.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise the host.
+ *  - Every argument is validated before anything is launched; a non-zero
+ *    return value is an ETATTN_ERR_* code and nothing was launched.  No C++
+ *    exception crosses this boundary.
+ *  - Supported: head dim D in {32, 64, 128}; the d-stride of every tensor is
+ *    1; all other strides and every base pointer are 16-byte aligned (TMA
+ *    rule); scale is finite and > 0.
+ *  - Empty work (B, Hq or N equal to 0; or no tokens) is a successful no-op.
+ */
+#ifndef ETATTN_H
+#define ETATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of q, k, v, o. */
+enum etattn_dtype { ETATTN_F16 = 0, ETATTN_BF16 = 1 };
+
+/* Status codes. */
+enum etattn_status {
+  ETATTN_OK = 0,
+  ETATTN_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
+  ETATTN_ERR_BAD_DTYPE = 2,    /* dtype is not ETATTN_F16 / ETATTN_BF16 */
+  ETATTN_ERR_BAD_SHAPE = 3,    /* negative size, D not in {32,64,128}, or a size beyond the limits */
+  ETATTN_ERR_BAD_HEADS = 4,    /* Hkv <= 0 or Hq not a multiple of Hkv */
+  ETATTN_ERR_BAD_STRIDE = 5,   /* d-stride != 1, negative stride, or a stride not a multiple of 16 bytes */
+  ETATTN_ERR_BAD_ALIGN = 6,    /* a base pointer is not 16-byte aligned */
+  ETATTN_ERR_ALIAS = 7,        /* o or lse overlaps an input, or o overlaps lse */
+  ETATTN_ERR_BAD_SCALE = 8,    /* scale is not finite or not > 0 */
+  ETATTN_ERR_BAD_SEQLENS = 9,  /* cu_seqlens not non-decreasing from 0 to total_tokens, or a length > max_seqlen */
+  ETATTN_ERR_LAUNCH = 10,      /* a CUDA runtime call failed (the CUDA error is in etattn_last_cuda_error) */
+  ETATTN_ERR_DEVICE = 11,      /* the device reported a failure (see etattn_read_device_status) */
+  ETATTN_ERR_NO_DEVICE = 12,   /* no sm_103 device is current */
+};
+
+/*
+ * attn_fwd: batched multi-head (optionally grouped-query) self-attention.
+ *
+ *   q  : logical [B, Hq,  N, D], element (b,h,n,d) at q[b*sq[0] + h*sq[1] + n*sq[2] + d*sq[3]]
+ *   k,v: logical [B, Hkv, N, D], strides sk / sv likewise
+ *   o  : logical [B, Hq,  N, D], strides so likewise
+ *   lse: [B, Hq, N] contiguous FP32 (or NULL)
+ *   strides: 16 int64 values, sq[4], sk[4], sv[4], so[4], each (b, h, n, d).
+ *            [B,H,N,D]-contiguous and [B,N,H,D]-contiguous storage are both
+ *            expressible; the d-stride must be 1.
+ *   causal : 0 = every key eligible; 1 = keys j <= i (diagonal included)
+ *   scale  : logit scale (commonly 1/sqrt(D))
+ * Limits: N <= 8,388,480; B*Hq <= 2^31-1.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int D, int dtype, const int64_t* strides, int causal, float scale, void* stream);
+
+/*
+ * attn_fwd_varlen: packed variable-length batch of num_seqs sequences.
+ *
+ *   q  : logical [T, Hq,  D], element (t,h,d) at q[t*sq[0] + h*sq[1] + d*sq[2]]
+ *   k,v: logical [T, Hkv, D]
+ *   o  : logical [T, Hq,  D]
+ *   lse: [Hq, T] contiguous FP32 (or NULL)
+ *   strides: 12 int64 values, sq[3], sk[3], sv[3], so[3], each (t, h, d).
+ *   cu_seqlens: DEVICE int32 [num_seqs + 1]; sequence s owns tokens
+ *            cu_seqlens[s] .. cu_seqlens[s+1]-1 and its logical positions
+ *            are 0 .. L_s-1.  It must be non-decreasing from 0 to T with
+ *            every L_s <= max_seqlen.
+ *   cu_seqlens_host: optional HOST mirror of cu_seqlens (may be NULL).  When
+ *            given it is validated before launch (ETATTN_ERR_BAD_SEQLENS);
+ *            otherwise the kernel checks each sequence it reads and, on a bad
+ *            entry, skips that sequence and records ETATTN_ERR_BAD_SEQLENS in
+ *            the device status word (see etattn_read_device_status).
+ * Limits: max_seqlen <= 8,388,480; num_seqs*Hq <= 2^31-1.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                    const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
+                    int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* etattn_status_string(int code);
+
+/* The cudaError_t value of the last ETATTN_ERR_LAUNCH on this thread (0 if none). */
+int etattn_last_cuda_error(void);
+
+/*
+ * Read the device status word of the current device that kernels set on a
+ * failure they detect themselves (a bounded wait that ran out, or a bad
+ * cu_seqlens entry).  Synchronises `stream`.  *out receives ETATTN_OK or the
+ * ETATTN_ERR_* code; when clear != 0 the word is reset to 0 afterwards.
+ * Returns ETATTN_OK or ETATTN_ERR_LAUNCH.
+ */
+int etattn_read_device_status(int* out, int clear, void* stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int etattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ETATTN_H */

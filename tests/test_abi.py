@@ -1,0 +1,149 @@
+"""CPU tests of the C-ABI library: it builds, loads, exports every function
+declared in include/etattn.h, and rejects invalid calls with the documented
+status codes before touching CUDA (so no GPU is needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_tiled_attention_19_gb300 import binding as B
+from exact_tiled_attention_19_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# Fake, 16-byte aligned, non-overlapping device addresses: validation never
+# dereferences them.
+Q, K, V, O, LSE = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def contiguous_strides(B_, H, N, D):
+    return [H * N * D, N * D, D, 1]
+
+
+def good_args(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=LSE, B=2, Hq=4, Hkv=2, N=100, D=64, dtype=1, causal=1, scale=0.125,
+             stream=0)
+    a.update(kw)
+    if "strides" not in a:
+        a["strides"] = (contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]) +
+                        contiguous_strides(a["B"], a["Hkv"], a["N"], a["D"]) * 2 +
+                        contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]))
+    return a
+
+
+def call(**kw):
+    a = good_args(**kw)
+    return B.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], a["D"],
+                      a["dtype"], a["strides"], a["causal"], a["scale"], a["stream"])
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "etattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", text)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    path = build_lib.build()
+    lib = ctypes.CDLL(path)
+    names = declared_functions()
+    assert {"attn_fwd", "attn_fwd_varlen", "etattn_status_string", "etattn_version"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/etattn.h but not exported"
+
+
+def test_status_strings_and_version():
+    for code in range(13):
+        s = B.etattn_status_string(code)
+        assert s and s != "unknown status"
+    assert B.etattn_status_string(999) == "unknown status"
+    assert B.etattn_version() >= 100
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), 2),
+    (dict(D=96), 3), (dict(D=256), 3), (dict(N=-1), 3), (dict(B=-1), 3), (dict(N=65535 * 128 + 1), 3),
+    (dict(Hkv=0), 4), (dict(Hkv=3), 4), (dict(Hq=4, Hkv=8), 4),
+    (dict(scale=0.0), 8), (dict(scale=-1.0), 8), (dict(scale=float("inf")), 8), (dict(scale=float("nan")), 8),
+    (dict(q=0), 1), (dict(o=0), 1), (dict(k=0), 1),
+    (dict(q=Q + 8), 6), (dict(o=O + 2), 6), (dict(lse=LSE + 2), 6),
+    (dict(o=Q + 64), 7), (dict(lse=K), 7), (dict(lse=O + 1024), 7),
+])
+def test_invalid_arguments_rejected(kw, code):
+    assert call(**kw) == code
+
+
+def test_stride_rules():
+    a = good_args()
+    s = list(a["strides"])
+    s[3] = 2  # q d-stride
+    assert call(strides=s) == 5
+    s = list(a["strides"])
+    s[2] = 60  # q n-stride of 120 bytes: not a multiple of 16
+    assert call(strides=s) == 5
+    s = list(a["strides"])
+    s[14] = -64  # o n-stride negative
+    assert call(strides=s) == 5
+    s = list(a["strides"])
+    s[5] = 0  # k head stride 0 with Hkv = 2 (broadcast) is refused
+    assert call(strides=s) == 5
+
+
+def test_null_strides_rejected():
+    lib = B.load_library()
+    rc = lib.attn_fwd(Q, K, V, O, LSE, 1, 1, 1, 8, 64, 0, None, 1, ctypes.c_float(0.1), None)
+    assert rc == 1
+
+
+def test_empty_work_is_a_noop_even_with_null_pointers():
+    assert call(N=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    assert call(B=0) == 0
+    assert call(Hq=0, Hkv=1) == 0
+
+
+def test_valid_call_without_gpu_reports_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call() == 12
+
+
+def varlen_call(cu_host=None, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=LSE, cu=0x60000000, num_seqs=3, max_seqlen=50, T=100, Hq=4, Hkv=4, D=128,
+             dtype=1, causal=1, scale=0.1, stream=0)
+    a.update(kw)
+    st = [a["Hq"] * a["D"], a["D"], 1, a["Hkv"] * a["D"], a["D"], 1, a["Hkv"] * a["D"], a["D"], 1,
+          a["Hq"] * a["D"], a["D"], 1]
+    host = 0
+    if cu_host is not None:
+        arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+        host = ctypes.addressof(arr)
+        a["_keep"] = arr
+    return B.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], host, a["num_seqs"],
+                             a["max_seqlen"], a["T"], a["Hq"], a["Hkv"], a["D"], a["dtype"], st, a["causal"],
+                             a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("cu,code", [
+    ([0, 30, 60, 100], 0), ([1, 30, 60, 100], 9), ([0, 30, 20, 100], 9), ([0, 30, 60, 99], 9),
+    ([0, 10, 20, 100], 9),  # last length 80 > max_seqlen 50
+])
+def test_varlen_host_seqlens_validation(cu, code):
+    import torch
+    rc = varlen_call(cu_host=cu)
+    if code == 0:
+        assert rc in (0, 12) if not torch.cuda.is_available() else rc == 0
+    else:
+        assert rc == code
+
+
+def test_varlen_argument_errors():
+    assert varlen_call(cu=0) == 1
+    assert varlen_call(D=48) == 3
+    assert varlen_call(Hkv=3) == 4
+    assert varlen_call(num_seqs=0) == 0
+    assert varlen_call(T=0, max_seqlen=0) == 0
+    assert varlen_call(cu=0x60000002) == 6

@@ -1,0 +1,151 @@
+"""GPU metamorphic and contract checks (bit-exact where the arithmetic is
+identical): future-value perturbation, layout and GQA equivalence, packed vs
+per-sequence calls, input preservation, non-default streams, NaN canaries
+around the outputs, determinism and the device status word."""
+
+import hashlib
+
+import pytest
+import torch
+
+from exact_tiled_attention_19_gb300 import binding
+from exact_tiled_attention_19_gb300 import workloads as W
+from tests.parity_helpers import rebuild_strided, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean():
+    yield
+    assert binding.etattn_read_device_status(clear=True) == 0
+
+
+def _digest(*ts):
+    h = hashlib.sha256()
+    for t in ts:
+        h.update(t.detach().contiguous().view(torch.uint8).cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+@pytest.mark.parametrize("i0", [0, 100, 127, 128, 300, 511])
+def test_future_value_perturbation_bit_exact(i0):
+    """Changing keys/values after position i0 leaves causal rows <= i0 bit-identical."""
+    inp = W.random_qkv(1, 2, 2, 512, 64, torch.float16, seed=7)
+    o1, l1 = run_gpu(inp, True)
+    g = torch.Generator().manual_seed(99)
+    k2, v2 = inp["k"].clone(), inp["v"].clone()
+    k2[:, :, i0 + 1:] = (torch.randn(k2[:, :, i0 + 1:].shape, generator=g) * 50).half()
+    v2[:, :, i0 + 1:] = (torch.randn(v2[:, :, i0 + 1:].shape, generator=g) * 50).half()
+    o2, l2 = run_gpu({"q": inp["q"], "k": k2, "v": v2}, True)
+    assert torch.equal(o1[:, :, : i0 + 1], o2[:, :, : i0 + 1])
+    assert torch.equal(l1[:, :, : i0 + 1], l2[:, :, : i0 + 1])
+    if i0 < 511:
+        assert not torch.equal(o1[:, :, i0 + 1:], o2[:, :, i0 + 1:])
+
+
+def test_transposed_layout_bit_identical():
+    a = W.random_qkv(2, 4, 4, 700, 128, torch.bfloat16, seed=8)
+    b = W.random_qkv(2, 4, 4, 700, 128, torch.bfloat16, seed=8, layout="bnhd")
+    oa, la = run_gpu(a, True)
+    ob, lb = run_gpu({k_: rebuild_strided(t) for k_, t in b.items()}, True)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_gqa_equals_repeated_kv_bit_identical():
+    inp = W.random_qkv(1, 8, 2, 400, 128, torch.bfloat16, seed=9)
+    o1, l1 = run_gpu(inp, True)
+    rep = {"q": inp["q"], "k": inp["k"].repeat_interleave(4, dim=1), "v": inp["v"].repeat_interleave(4, dim=1)}
+    o2, l2 = run_gpu(rep, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_varlen_equals_per_sequence_calls_bit_identical():
+    lengths = [300, 1, 129, 0, 512]
+    inp = W.random_varlen(lengths, 4, 2, 128, torch.bfloat16, seed=10)
+    o, lse = run_gpu(inp, True)
+    cu = inp["cu_seqlens"].tolist()
+    for s, L in enumerate(lengths):
+        if L == 0:
+            continue
+        t0 = cu[s]
+        per = {n: inp[n][t0:t0 + L].permute(1, 0, 2).unsqueeze(0) for n in ("q", "k", "v")}
+        o_s, l_s = run_gpu({n: t.contiguous() for n, t in per.items()}, True)
+        assert torch.equal(o_s[0].permute(1, 0, 2), o[t0:t0 + L])
+        assert torch.equal(l_s[0], lse[:, t0:t0 + L])
+
+
+def test_inputs_unchanged_and_deterministic():
+    inp = W.random_qkv(2, 4, 2, 500, 64, torch.bfloat16, seed=11)
+    dev = {n: t.cuda() for n, t in inp.items()}
+    before = _digest(dev["q"], dev["k"], dev["v"])
+    o1, l1 = binding.attention(dev["q"], dev["k"], dev["v"], causal=True)
+    o2, l2 = binding.attention(dev["q"], dev["k"], dev["v"], causal=True)
+    torch.cuda.synchronize()
+    assert _digest(dev["q"], dev["k"], dev["v"]) == before
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_nondefault_stream():
+    inp = W.random_qkv(1, 4, 4, 1000, 128, torch.bfloat16, seed=12)
+    dev = {n: t.cuda() for n, t in inp.items()}
+    o_ref, l_ref = binding.attention(dev["q"], dev["k"], dev["v"], causal=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o_s, l_s = binding.attention(dev["q"], dev["k"], dev["v"], causal=True, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(o_ref, o_s) and torch.equal(l_ref, l_s)
+
+
+def test_nan_canary_outputs_written_exactly():
+    """Outputs live inside NaN-filled buffers; every element of the output
+    view is written and nothing outside it is touched."""
+    B_, H, N, D = 2, 3, 259, 64
+    inp = W.random_qkv(B_, H, H, N, D, torch.float16, seed=13)
+    dev = {n: t.cuda() for n, t in inp.items()}
+    big = torch.full((B_, H, N + 9, D + 8), float("nan"), dtype=torch.float16, device="cuda")
+    o_view = big[:, :, 4:4 + N, :D]
+    lse_big = torch.full((B_ * H * N + 64,), float("nan"), dtype=torch.float32, device="cuda")
+    lse_view = lse_big[32:32 + B_ * H * N].view(B_, H, N)
+    binding.attention(dev["q"], dev["k"], dev["v"], causal=True, out=o_view, lse=lse_view)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o_view).any() and not torch.isnan(lse_view).any()
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[:, :, 4:4 + N, :D] = False
+    assert torch.isnan(big[mask]).all()
+    assert torch.isnan(lse_big[:32]).all() and torch.isnan(lse_big[32 + B_ * H * N:]).all()
+    o_ref, l_ref = run_gpu(inp, True)
+    assert torch.equal(o_view, o_ref) and torch.equal(lse_view, l_ref)
+
+
+def test_varlen_nan_canary_and_empty_sequences():
+    lengths = [0, 5, 0, 200, 0]
+    inp = W.random_varlen(lengths, 2, 2, 32, torch.float16, seed=14)
+    T = sum(lengths)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
+    o = torch.full((T, 2, 32), float("nan"), dtype=torch.float16, device="cuda")
+    lse = torch.full((2, T), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attention_varlen(dev["q"], dev["k"], dev["v"], inp["cu_seqlens"].cuda(), 200, causal=True,
+                             out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+
+
+def test_device_checks_bad_seqlens_without_host_mirror():
+    """A decreasing cu_seqlens entry seen only on the device is reported
+    through the status word; the affected sequence is skipped."""
+    inp = W.random_varlen([64, 64], 1, 1, 64, torch.float16, seed=15)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
+    bad = torch.tensor([0, 100, 50], dtype=torch.int32, device="cuda")  # sequence 1 has length -50
+    o = torch.zeros((128, 1, 64), dtype=torch.float16, device="cuda")
+    binding.attention_varlen(dev["q"], dev["k"], dev["v"], bad, 100, causal=True, out=o)
+    assert binding.etattn_read_device_status(clear=True) == 9
+    assert binding.etattn_read_device_status(clear=True) == 0
+
+
+def test_status_error_is_raised_for_bad_call():
+    q = torch.zeros((1, 1, 16, 48), dtype=torch.float16, device="cuda")
+    with pytest.raises(binding.EtattnError):
+        binding.attention(q, q, q)
