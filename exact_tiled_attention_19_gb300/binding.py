@@ -64,6 +64,10 @@ def load_library(path: str | None = None):
         lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                                         _int, _i64p, _int, ctypes.c_float, _vp]
         lib.attn_fwd_varlen.restype = _int
+        lib.attn_fwd_host.argtypes = [_vp] * 10 + [_int] * 7 + [ctypes.c_float, _vp]
+        lib.attn_fwd_host.restype = _int
+        lib.attn_fwd_varlen_host.argtypes = [_vp] * 12 + [_int] * 8 + [ctypes.c_float, _vp]
+        lib.attn_fwd_varlen_host.restype = _int
         lib.etattn_status_string.argtypes = [_int]
         lib.etattn_status_string.restype = ctypes.c_char_p
         lib.etattn_last_cuda_error.argtypes = []
@@ -98,6 +102,27 @@ def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, cu_seqlens_host, num_seqs, max_
     return lib.attn_fwd_varlen(q or None, k or None, v or None, o or None, lse or None, cu_seqlens or None,
                                cu_seqlens_host or None, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D, dtype,
                                _strides_arg(strides), causal, scale, stream or None)
+
+
+def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, D,
+                  dtype, causal, scale, stream):
+    """C ``attn_fwd_host``: host and device buffer addresses as ints."""
+    lib = load_library()
+    return lib.attn_fwd_host(q_host or None, k_host or None, v_host or None, o_host or None, lse_host or None,
+                             q_dev or None, k_dev or None, v_dev or None, o_dev or None, lse_dev or None, B, Hq,
+                             Hkv, N, D, dtype, causal, scale, stream or None)
+
+
+def attn_fwd_varlen_host(q_host, k_host, v_host, o_host, lse_host, cu_seqlens_host, q_dev, k_dev, v_dev, o_dev,
+                         lse_dev, cu_seqlens_dev, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D, dtype, causal,
+                         scale, stream):
+    """C ``attn_fwd_varlen_host``: host and device buffer addresses as ints."""
+    lib = load_library()
+    return lib.attn_fwd_varlen_host(q_host or None, k_host or None, v_host or None, o_host or None,
+                                    lse_host or None, cu_seqlens_host or None, q_dev or None, k_dev or None,
+                                    v_dev or None, o_dev or None, lse_dev or None, cu_seqlens_dev or None,
+                                    num_seqs, max_seqlen, total_tokens, Hq, Hkv, D, dtype, causal, scale,
+                                    stream or None)
 
 
 def etattn_status_string(code: int) -> str:

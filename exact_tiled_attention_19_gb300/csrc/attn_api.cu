@@ -187,10 +187,11 @@ bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 128; }
 
 using namespace etattn;
 
-extern "C" {
+namespace {
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
-             int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
+// Validates every argument; launches only when do_launch is set.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int D,
+             int dtype, const int64_t* strides, int causal, float scale, void* stream, bool do_launch) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (B < 0 || Hq < 0 || N < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
   if (N > kMaxTokens || (int64_t)B * Hq > INT_MAX) return ETATTN_ERR_BAD_SHAPE;
@@ -213,6 +214,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   for (const View* t : {&vq, &vk, &vv})
     if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
   if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
+  if (!do_launch) return ETATTN_OK;
 
   int dev = 0;
   int* status = nullptr;
@@ -249,9 +251,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ETATTN_OK;
 }
 
-int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
-                    const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
-                    int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
+int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq, int Hkv,
+                int D, int dtype, const int64_t* strides, int causal, float scale, void* stream, bool do_launch) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (num_seqs < 0 || max_seqlen < 0 || total_tokens < 0 || Hq < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
   if (max_seqlen > kMaxTokens || (int64_t)num_seqs * Hq > INT_MAX) return ETATTN_ERR_BAD_SHAPE;
@@ -283,6 +285,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   for (const View* t : {&vq, &vk, &vv})
     if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
   if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
+  if (!do_launch) return ETATTN_OK;
 
   int dev = 0;
   int* status = nullptr;
@@ -315,6 +318,80 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   const unsigned gx = (unsigned)(num_seqs * Hq), gy = (unsigned)((max_seqlen + 127) / 128);
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ETATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, D, dtype, strides, causal, scale, stream, true);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
+                    const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
+                    int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
+  return varlen_impl(q, k, v, o, lse, cu_seqlens, cu_seqlens_host, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D,
+                     dtype, strides, causal, scale, stream, true);
+}
+
+int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                  void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int Hq, int Hkv, int N,
+                  int D, int dtype, int causal, float scale, void* stream) {
+  if ((lse_host == nullptr) != (lse_dev == nullptr)) return ETATTN_ERR_NULL_PTR;
+  const int64_t st[16] = {(int64_t)Hq * N * D,  (int64_t)N * D, D, 1, (int64_t)Hkv * N * D, (int64_t)N * D, D, 1,
+                          (int64_t)Hkv * N * D, (int64_t)N * D, D, 1, (int64_t)Hq * N * D,  (int64_t)N * D, D, 1};
+  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, D, dtype, st, causal, scale, stream,
+                        false))
+    return rc;
+  if (B == 0 || Hq == 0 || N == 0) return ETATTN_OK;
+  if (!q_host || !k_host || !v_host || !o_host) return ETATTN_ERR_NULL_PTR;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nq = (size_t)B * Hq * N * D * 2, nkv = (size_t)B * Hkv * N * D * 2;
+  cudaError_t e = cudaMemcpyAsync(q_dev, q_host, nq, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(k_dev, k_host, nkv, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v_dev, v_host, nkv, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, D, dtype, st, causal, scale, stream,
+                        true))
+    return rc;
+  e = cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && lse_host)
+    e = cudaMemcpyAsync(lse_host, lse_dev, (size_t)B * Hq * N * sizeof(float), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ETATTN_OK;
+}
+
+int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                         const int32_t* cu_seqlens_host, void* q_dev, void* k_dev, void* v_dev, void* o_dev,
+                         float* lse_dev, int32_t* cu_seqlens_dev, int num_seqs, int max_seqlen, int total_tokens,
+                         int Hq, int Hkv, int D, int dtype, int causal, float scale, void* stream) {
+  if ((lse_host == nullptr) != (lse_dev == nullptr)) return ETATTN_ERR_NULL_PTR;
+  if (cu_seqlens_host == nullptr) return ETATTN_ERR_NULL_PTR;
+  const int64_t st[12] = {(int64_t)Hq * D, D, 1, (int64_t)Hkv * D, D, 1, (int64_t)Hkv * D, D, 1, (int64_t)Hq * D, D, 1};
+  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, cu_seqlens_host, num_seqs,
+                           max_seqlen, total_tokens, Hq, Hkv, D, dtype, st, causal, scale, stream, false))
+    return rc;
+  if (num_seqs == 0 || Hq == 0 || total_tokens == 0 || max_seqlen == 0) return ETATTN_OK;
+  if (!q_host || !k_host || !v_host || !o_host) return ETATTN_ERR_NULL_PTR;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t T = (size_t)total_tokens;
+  const size_t nq = T * Hq * D * 2, nkv = T * Hkv * D * 2;
+  cudaError_t e = cudaMemcpyAsync(cu_seqlens_dev, cu_seqlens_host, (size_t)(num_seqs + 1) * sizeof(int32_t),
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(q_dev, q_host, nq, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(k_dev, k_host, nkv, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v_dev, v_host, nkv, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, nullptr, num_seqs, max_seqlen,
+                           total_tokens, Hq, Hkv, D, dtype, st, causal, scale, stream, true))
+    return rc;
+  e = cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && lse_host)
+    e = cudaMemcpyAsync(lse_host, lse_dev, T * Hq * sizeof(float), cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }

@@ -106,6 +106,38 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
                     int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream);
 
+/*
+ * attn_fwd_host: attn_fwd for callers whose q, k, v live in HOST memory and
+ * who want O (and lse) back in host memory, all in one call.
+ *
+ *   *_host: HOST buffers, contiguous [B,H,N,D] (q, o: H = Hq; k, v: H = Hkv)
+ *           and lse_host [B,Hq,N] FP32 (or NULL).  Pinned (page-locked)
+ *           memory lets the copies run asynchronously; pageable memory works
+ *           but the copies then block the calling thread.
+ *   *_dev : caller-owned DEVICE buffers of the same sizes and layouts; the
+ *           inputs are staged there and the outputs computed there.  lse_dev
+ *           must be NULL exactly when lse_host is NULL.
+ * On `stream` the call enqueues: three host-to-device copies, the attention
+ * kernel, and the device-to-host copies of O and lse.  It returns once they
+ * are enqueued; synchronise `stream` before reading o_host / lse_host.
+ * Arguments are validated (as for attn_fwd, on the device buffers) before
+ * anything is enqueued.  Nothing is allocated.
+ */
+int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                  void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int Hq, int Hkv, int N,
+                  int D, int dtype, int causal, float scale, void* stream);
+
+/*
+ * attn_fwd_varlen_host: attn_fwd_varlen with host buffers, as attn_fwd_host.
+ *   q/k/v/o host and device buffers: contiguous [T,H,D]; lse [Hq,T] FP32 or NULL.
+ *   cu_seqlens_host (required) is validated on the host and copied to the
+ *   caller-owned device buffer cu_seqlens_dev (int32 [num_seqs+1]).
+ */
+int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                         const int32_t* cu_seqlens_host, void* q_dev, void* k_dev, void* v_dev, void* o_dev,
+                         float* lse_dev, int32_t* cu_seqlens_dev, int num_seqs, int max_seqlen, int total_tokens,
+                         int Hq, int Hkv, int D, int dtype, int causal, float scale, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* etattn_status_string(int code);
 

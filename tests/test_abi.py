@@ -147,3 +147,26 @@ def test_varlen_argument_errors():
     assert varlen_call(num_seqs=0) == 0
     assert varlen_call(T=0, max_seqlen=0) == 0
     assert varlen_call(cu=0x60000002) == 6
+
+
+def test_host_entry_points_validate_before_copying():
+    H = 0x70000000  # fake host addresses (never touched: validation fails first or no GPU)
+    # lse host/device must be both given or both NULL
+    assert B.attn_fwd_host(H, H + 0x100000, H + 0x200000, H + 0x300000, H + 0x400000, Q, K, V, O, 0, 1, 2, 2, 64,
+                           64, 1, 1, 0.125, 0) == 1
+    assert B.attn_fwd_host(H, H, H, H, 0, Q, K, V, O, 0, 1, 2, 2, 64, 48, 1, 1, 0.125, 0) == 3
+    assert B.attn_fwd_host(H, H, H, H, 0, Q, K, V, Q + 64, 0, 1, 2, 2, 64, 64, 1, 1, 0.125, 0) == 7
+    assert B.attn_fwd_host(0, 0, 0, 0, 0, Q, K, V, O, 0, 0, 2, 2, 64, 64, 1, 1, 0.125, 0) == 0  # empty
+    cu = (ctypes.c_int32 * 3)(0, 10, 30)
+    cu_bad = (ctypes.c_int32 * 3)(0, 40, 30)
+    args = dict(num_seqs=2, max_seqlen=20, T=30, Hq=2, Hkv=2, D=64, dtype=1, causal=1, scale=0.1)
+
+    def vh(cu_arr, **kw):
+        a = dict(args, **kw)
+        return B.attn_fwd_varlen_host(H, H, H, H, 0, ctypes.addressof(cu_arr) if cu_arr is not None else 0, Q, K,
+                                      V, O, 0, 0x60000000, a["num_seqs"], a["max_seqlen"], a["T"], a["Hq"],
+                                      a["Hkv"], a["D"], a["dtype"], a["causal"], a["scale"], 0)
+    assert vh(None) == 1
+    assert vh(cu_bad) == 9
+    assert vh(cu, Hkv=3) == 4
+    assert vh(cu, scale=-1.0) == 8

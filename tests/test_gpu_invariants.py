@@ -149,3 +149,42 @@ def test_status_error_is_raised_for_bad_call():
     q = torch.zeros((1, 1, 16, 48), dtype=torch.float16, device="cuda")
     with pytest.raises(binding.EtattnError):
         binding.attention(q, q, q)
+
+
+def test_host_buffer_entry_points_match_device_path():
+    """attn_fwd_host / attn_fwd_varlen_host (pinned host in, host out) give
+    bit-identical results to the device-resident calls."""
+    s = torch.cuda.Stream()
+    # batched
+    inp = W.random_qkv(2, 4, 2, 300, 128, torch.bfloat16, seed=16)
+    o_ref, l_ref = run_gpu(inp, True)
+    pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+    dq, dk, dv = (torch.empty_like(pin[n], device="cuda") for n in ("q", "k", "v"))
+    do, dl = torch.empty_like(o_ref), torch.empty_like(l_ref)
+    oh = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+    lh = torch.empty(l_ref.shape, dtype=torch.float32).pin_memory()
+    rc = binding.attn_fwd_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(), oh.data_ptr(),
+                               lh.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(),
+                               dl.data_ptr(), 2, 4, 2, 300, 128, 1, 1, 1 / 128 ** 0.5, s.cuda_stream)
+    assert rc == 0
+    s.synchronize()
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+    # packed
+    lengths = [100, 0, 257]
+    inp = W.random_varlen(lengths, 2, 1, 64, torch.float16, seed=17)
+    o_ref, l_ref = run_gpu(inp, True)
+    T = sum(lengths)
+    pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+    cu_h = inp["cu_seqlens"].pin_memory()
+    dq, dk, dv = (torch.empty_like(pin[n], device="cuda") for n in ("q", "k", "v"))
+    do, dl = torch.empty_like(o_ref), torch.empty_like(l_ref)
+    cu_d = torch.empty(len(lengths) + 1, dtype=torch.int32, device="cuda")
+    oh = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+    lh = torch.empty(l_ref.shape, dtype=torch.float32).pin_memory()
+    rc = binding.attn_fwd_varlen_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
+                                      oh.data_ptr(), lh.data_ptr(), cu_h.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                      dv.data_ptr(), do.data_ptr(), dl.data_ptr(), cu_d.data_ptr(), len(lengths),
+                                      max(lengths), T, 2, 1, 64, 0, 1, 1 / 8.0, s.cuda_stream)
+    assert rc == 0
+    s.synchronize()
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
