@@ -245,7 +245,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  const unsigned gx = (unsigned)(B * Hq), gy = (unsigned)((N + 127) / 128);
+  const unsigned gx = (unsigned)(B * Hq), gy = (unsigned)((N + 255) / 256);
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
@@ -316,7 +316,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  const unsigned gx = (unsigned)(num_seqs * Hq), gy = (unsigned)((max_seqlen + 127) / 128);
+  const unsigned gx = (unsigned)(num_seqs * Hq), gy = (unsigned)((max_seqlen + 255) / 256);
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;

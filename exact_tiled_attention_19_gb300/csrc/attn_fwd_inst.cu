@@ -32,6 +32,12 @@ cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CU
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
+    // The kernel re-splits its registers between warpgroups (setmaxnreg); the
+    // split is only valid if every thread launches with LAUNCH_REGS registers.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);

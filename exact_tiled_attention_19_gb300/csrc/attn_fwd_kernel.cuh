@@ -1,6 +1,6 @@
-// Exact streaming attention forward, one 128-row query tile per CTA, for
-// sm_103a: TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating in tensor
-// memory, and warp-specialised roles.
+// Exact streaming attention forward for sm_103a: TMA-staged Q/K/V tiles,
+// tcgen05 MMAs accumulating in tensor memory, warp-specialised roles, and two
+// 128-row query sub-tiles per CTA that take turns on the tensor core.
 //
 // Method ("Intermediate and advanced extension", workshop row "Streaming
 // attention" and "Logic review before implementation"): S = Q K^T is formed
@@ -11,17 +11,30 @@
 // mask keeps the diagonal; key tiles wholly in a row block's future are never
 // visited.  The epilogue writes O / l and lse = scale*m + ln l.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t of the tile (tensor-memory
-//              lane t); reads S, updates (m, l), writes P to tensor memory,
-//              rescales its O row when needed, and runs the epilogue.
-//   warp 4     TMA producer: Q once, then K_j and V_j into two-stage rings.
-//   warp 5     tensor-memory allocator and MMA issuer.
+// A CTA owns 256 query rows as two sub-tiles (rows [0,128) and [128,256) of
+// the block).  Both read the same K/V tiles from shared memory.
+//
+// Roles (384 threads = 3 warpgroups):
+//   warpgroup 0 (warps 0-3)  softmax + correction + epilogue of sub-tile 0:
+//                            thread t owns row t (tensor-memory lane t).
+//   warpgroup 1 (warps 4-7)  the same for sub-tile 1.
+//   warp 8                   TMA producer: Q0, Q1 once, then K_j, V_j into
+//                            two-stage rings.
+//   warp 9                   tensor-memory allocator and MMA issuer.
+//   warps 10-11              no work (they complete warpgroup 2).
 //
 // Tensor memory (512 columns x 128 lanes, FP32 cells):
-//   [  0,128) S buffer 0     [128,256) S buffer 1
-//   [256,256+D) O accumulator
-//   [384,448) P buffer 0     [448,512) P buffer 1   (two 16-bit values per cell)
+//   S_s  = columns [128 s, 128 s + 128)         score tile of sub-tile s
+//   P_s  = columns [128 s, 128 s + 64)          P overwrites its own S (two 16-bit values per cell)
+//   O_s  = columns [256 + 128 s, 256 + 128 s + D)
+//
+// MMA issue order per key tile j >= 1:
+//   PV_0(j-1), S_0(j), PV_1(j-1), S_1(j)
+// so the softmax of one sub-tile overlaps two MMAs of the other, and a
+// commit on S_s(j) also covers PV_s(j-1) (a commit tracks every earlier
+// tcgen05 operation of the issuing thread): when the softmax of sub-tile s
+// sees S_s(j), O_s is up to date and may be rescaled.  S_s(j+1) overwrites
+// P_s(j) only after PV_s(j), which was issued before it by the same thread.
 //
 // Lazy rescaling: m is only moved when the tile maximum exceeds it by more
 // than 8 in log2 units; until then P = exp2(scale*log2e*(s - m)) <= 256, which
@@ -66,56 +79,75 @@ __device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map,
 
 template <int D>
 struct TileCfg {
-  static constexpr int BM = 128;                       // query rows per tile
+  static constexpr int BM = 128;                       // query rows per sub-tile
+  static constexpr int BLOCK_M = 2 * BM;               // query rows per CTA
   static constexpr int BN = 128;                       // keys per tile
   static constexpr int SW_ELEMS = D >= 64 ? 64 : 32;   // elements per swizzled smem row
   static constexpr int SW_BYTES = SW_ELEMS * 2;        // 128 B (D >= 64) or 64 B (D = 32)
   static constexpr uint32_t SWIZZLE = D >= 64 ? kSw128 : kSw64;
   static constexpr int NCHUNK = D / SW_ELEMS;          // TMA boxes per tile along d
   static constexpr int KSTEPS_PER_CHUNK = SW_ELEMS / 16;
-  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int Q_BYTES = BM * D * 2;           // one sub-tile
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int STAGES = 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_V = Q_BYTES + STAGES * KV_BYTES;
-  static constexpr int SMEM_BYTES = Q_BYTES + 2 * STAGES * KV_BYTES + 1024;  // + alignment slack
+  static constexpr int OFF_Q = 0;                      // Q_0 then Q_1
+  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int SMEM_BYTES = OFF_V + STAGES * KV_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t SBO = 8 * SW_BYTES;        // stride between 8-row swizzle atoms
-  static constexpr uint32_t TM_S0 = 0, TM_O = 256, TM_P0 = 384;
-  static constexpr int THREADS = 192;
+  static constexpr uint32_t TM_S = 0, TM_O = 256;      // + 128 * sub-tile
+  static constexpr int THREADS = 384;
+  // Register split: 384 threads launch with LAUNCH_REGS each; warpgroup 2
+  // (TMA + MMA) shrinks to CTRL_REGS so that the two softmax warpgroups can
+  // grow to SOFTMAX_REGS.  128*CTRL_REGS + 256*SOFTMAX_REGS == 384*LAUNCH_REGS.
+  static constexpr int LAUNCH_REGS = 168;
+  static constexpr int CTRL_REGS = 56;
+  static constexpr int SOFTMAX_REGS = 224;
+  static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS, "register split over budget");
 };
 
 __device__ __forceinline__ void fence_regs32(uint32_t* r) {
   asm volatile("" : ETATTN_RW8(r, 0), ETATTN_RW8(r, 8), ETATTN_RW8(r, 16), ETATTN_RW8(r, 24));
 }
 
-template <int D>
 struct SmemBarriers {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t s_full[2];            // per sub-tile: S_s(j) is in tensor memory (and PV_s(j-1) is done)
+  uint64_t p_full[2];            // per sub-tile: P_s(j) written and O_s corrected
+  uint64_t o_done[2];            // per sub-tile: last PV_s has completed
   uint32_t tmem_base;
+};
+
+// Per-CTA work description shared by all roles.
+struct Unit {
+  int h, hk, b, bcoord;          // query head, kv head, batch/sequence index, batch coordinate of the maps
+  int tok0;                      // first token of the sequence (packed batch), else 0
+  int L;                         // sequence length
+  int row0;                      // first query row (logical position) of sub-tile 0
+  int n[2];                      // key tiles visited by sub-tile 0 / 1 (0 = sub-tile idle)
+  int n_max;
 };
 
 // ----------------------------------------------------------------- producer
 template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                              const CUtensorMap* tmV, SmemBarriers<D>& sb, uint8_t* smem,
-                                              int q_row0, int kv_row0, int h, int hk, int bcoord, int n_kv,
-                                              int hn_swapped, int* status) {
+                                              const CUtensorMap* tmV, SmemBarriers& sb, uint8_t* smem,
+                                              const Unit u, int hn_swapped, int* status) {
   using C = TileCfg<D>;
   const int lane = threadIdx.x & 31;
   const bool swq = hn_swapped & 1, swk = (hn_swapped >> 1) & 1, swv = (hn_swapped >> 2) & 1;
   if (lane == 0) {
-    mbar_arrive_expect_tx(&sb.q_full, C::Q_BYTES);
+    mbar_arrive_expect_tx(&sb.q_full, 2 * C::Q_BYTES);
 #pragma unroll
-    for (int c = 0; c < C::NCHUNK; ++c)
-      tma_load_tile(smem + C::OFF_Q + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full, c * C::SW_ELEMS, q_row0, h,
-                    bcoord, swq);
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int c = 0; c < C::NCHUNK; ++c)
+        tma_load_tile(smem + C::OFF_Q + s * C::Q_BYTES + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full,
+                      c * C::SW_ELEMS, u.tok0 + u.row0 + s * C::BM, u.h, u.bcoord, swq);
   }
-  for (int j = 0; j < n_kv; ++j) {
+  for (int j = 0; j < u.n_max; ++j) {
     const int st = j & 1;
     const uint32_t ph_prev = ((j - 2) >> 1) & 1;
     if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sb.k_empty[st], ph_prev, status))) return;
@@ -124,7 +156,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_K + st * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmK, &sb.k_full[st],
-                      c * C::SW_ELEMS, kv_row0 + j * C::BN, hk, bcoord, swk);
+                      c * C::SW_ELEMS, u.tok0 + j * C::BN, u.hk, u.bcoord, swk);
     }
     if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sb.v_empty[st], ph_prev, status))) return;
     if (lane == 0) {
@@ -132,78 +164,100 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_V + st * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmV, &sb.v_full[st],
-                      c * C::SW_ELEMS, kv_row0 + j * C::BN, hk, bcoord, swv);
+                      c * C::SW_ELEMS, u.tok0 + j * C::BN, u.hk, u.bcoord, swv);
     }
     __syncwarp();
   }
 }
 
 // ----------------------------------------------------------------- MMA issuer
+// S_s = Q_s K^T: both K-major (d contiguous); a 16-element step moves 32 bytes
+// inside a swizzled row, and a new d-chunk starts a new TMA box.
 template <int D>
-__device__ __forceinline__ bool issue_pv(SmemBarriers<D>& sb, uint8_t* smem, uint32_t tmem, int i,
-                                         uint32_t idesc_pv, int* status) {
+__device__ __forceinline__ void issue_s(uint8_t* smem, uint32_t tmem, int s, int st, uint32_t idesc) {
   using C = TileCfg<D>;
-  const int st = i & 1;
-  const uint32_t ph = (i >> 1) & 1;
-  bool ok = mbar_wait(&sb.v_full[st], ph, status) && mbar_wait(&sb.p_full[st], ph, status);
-  if (!__all_sync(0xffffffffu, ok)) return false;
-  tc_fence_after();
-  if ((threadIdx.x & 31) == 0) {
-    const uint32_t v_base = smem_u32(smem + C::OFF_V + st * C::KV_BYTES);
-    const uint32_t p_base = tmem + C::TM_P0 + st * 64;
+  const uint32_t q_base = smem_u32(smem + C::OFF_Q + s * C::Q_BYTES);
+  const uint32_t k_base = smem_u32(smem + C::OFF_K + st * C::KV_BYTES);
 #pragma unroll
-    for (int kk = 0; kk < C::BN / 16; ++kk) {
-      // V is MN-major (d contiguous): 16 keys per step = 16 swizzled rows;
-      // LBO steps between d-chunks, SBO between 8-row groups.
-      const uint64_t vdesc = smem_desc(v_base + kk * 16 * C::SW_BYTES, C::BN * C::SW_BYTES, C::SBO, C::SWIZZLE);
-      mma_ts(tmem + C::TM_O, p_base + kk * 8, vdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-    }
-    mma_commit(&sb.pv_done[st]);
-    mma_commit(&sb.v_empty[st]);
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int c = kk / C::KSTEPS_PER_CHUNK, w = kk % C::KSTEPS_PER_CHUNK;
+    const uint64_t qdesc = smem_desc(q_base + c * C::BM * C::SW_BYTES + w * 32, 16, C::SBO, C::SWIZZLE);
+    const uint64_t kdesc = smem_desc(k_base + c * C::BN * C::SW_BYTES + w * 32, 16, C::SBO, C::SWIZZLE);
+    mma_ss(tmem + C::TM_S + s * 128, qdesc, kdesc, idesc, kk > 0 ? 1u : 0u);
   }
-  __syncwarp();
-  return true;
+}
+
+// O_s (+)= P_s V: A = P_s from tensor memory (8 cells = 16 keys per step),
+// B = V MN-major (d contiguous): 16 keys = 16 swizzled rows per step; LBO
+// steps between d-chunks, SBO between 8-row groups.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint8_t* smem, uint32_t tmem, int s, int st, bool accumulate,
+                                         uint32_t idesc) {
+  using C = TileCfg<D>;
+  const uint32_t v_base = smem_u32(smem + C::OFF_V + st * C::KV_BYTES);
+  const uint32_t p_base = tmem + C::TM_S + s * 128;
+#pragma unroll
+  for (int kk = 0; kk < C::BN / 16; ++kk) {
+    const uint64_t vdesc = smem_desc(v_base + kk * 16 * C::SW_BYTES, C::BN * C::SW_BYTES, C::SBO, C::SWIZZLE);
+    mma_ts(tmem + C::TM_O + s * 128, p_base + kk * 8, vdesc, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 template <int D>
-__device__ __forceinline__ void mma_role(SmemBarriers<D>& sb, uint8_t* smem, uint32_t tmem, int n_kv,
+__device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
-  using C = TileCfg<D>;
-  if (!__all_sync(0xffffffffu, mbar_wait(&sb.q_full, 0, status))) return;
-  const uint32_t q_base = smem_u32(smem + C::OFF_Q);
-  for (int j = 0; j < n_kv; ++j) {
-    const int st = j & 1;
-    bool ok = mbar_wait(&sb.k_full[st], (j >> 1) & 1, status);
-    if (j >= 2) ok = ok && mbar_wait(&sb.s_empty[st], ((j - 2) >> 1) & 1, status);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    tc_fence_after();
-    if ((threadIdx.x & 31) == 0) {
-      const uint32_t k_base = smem_u32(smem + C::OFF_K + st * C::KV_BYTES);
+  constexpr uint32_t FULL = 0xffffffffu;
+  const bool leader = (threadIdx.x & 31) == 0;
+  if (!__all_sync(FULL, mbar_wait(&sb.q_full, 0, status) && mbar_wait(&sb.k_full[0], 0, status))) return;
+  tc_fence_after();
+  if (leader) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        // Q and K are K-major (d contiguous): a 16-element step moves 32 bytes
-        // inside a swizzled row, and a new d-chunk starts a new box.
-        const int c = kk / C::KSTEPS_PER_CHUNK, w = kk % C::KSTEPS_PER_CHUNK;
-        const uint64_t qdesc = smem_desc(q_base + c * C::BM * C::SW_BYTES + w * 32, 16, C::SBO, C::SWIZZLE);
-        const uint64_t kdesc = smem_desc(k_base + c * C::BN * C::SW_BYTES + w * 32, 16, C::SBO, C::SWIZZLE);
-        mma_ss(tmem + C::TM_S0 + st * 128, qdesc, kdesc, idesc_s, kk > 0 ? 1u : 0u);
+    for (int s = 0; s < 2; ++s) {
+      if (u.n[s] > 0) {
+        issue_s<D>(smem, tmem, s, 0, idesc_s);
+        mma_commit(&sb.s_full[s]);
       }
-      mma_commit(&sb.s_full[st]);
-      mma_commit(&sb.k_empty[st]);
     }
+    mma_commit(&sb.k_empty[0]);
+  }
+  __syncwarp();
+  for (int j = 1; j <= u.n_max; ++j) {
+    const int i = j - 1;  // key tile whose PV products are issued in this step
+    const bool has_k = j < u.n_max;
+    bool ok = mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status);
+    if (has_k) ok = ok && mbar_wait(&sb.k_full[j & 1], (j >> 1) & 1, status);
+    if (!__all_sync(FULL, ok)) return;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (i < u.n[s]) {
+        if (!__all_sync(FULL, mbar_wait(&sb.p_full[s], i & 1, status))) return;
+        tc_fence_after();
+        if (leader) {
+          issue_pv<D>(smem, tmem, s, i & 1, i > 0, idesc_pv);
+          if (i == u.n[s] - 1) mma_commit(&sb.o_done[s]);
+        }
+      }
+      if (s == 1 && leader) mma_commit(&sb.v_empty[i & 1]);  // both PV products of tile i issued
+      if (j < u.n[s] && leader) {
+        issue_s<D>(smem, tmem, s, j & 1, idesc_s);
+        mma_commit(&sb.s_full[s]);
+      }
+      __syncwarp();
+    }
+    if (has_k && leader) mma_commit(&sb.k_empty[j & 1]);
     __syncwarp();
-    if (j >= 1 && !issue_pv<D>(sb, smem, tmem, j - 1, idesc_pv, status)) return;
   }
-  if (!issue_pv<D>(sb, smem, tmem, n_kv - 1, idesc_pv, status)) return;
   // Drain: wait for the commit arrivals nobody else consumes (the last two
-  // iterations' stage releases and PV completions) so that no arrival can
-  // land in shared memory after the CTA exits.
-  for (int i = n_kv >= 2 ? n_kv - 2 : 0; i < n_kv; ++i) {
-    const uint32_t ph = (i >> 1) & 1;
-    const bool ok = mbar_wait(&sb.k_empty[i & 1], ph, status) && mbar_wait(&sb.v_empty[i & 1], ph, status) &&
-                    mbar_wait(&sb.pv_done[i & 1], ph, status);
-    if (!__all_sync(0xffffffffu, ok)) return;
+  // tiles' stage releases, and the final PV of an idle-epilogue sub-tile) so
+  // that no arrival can land in shared memory after the CTA exits.
+  for (int t = u.n_max >= 2 ? u.n_max - 2 : 0; t < u.n_max; ++t) {
+    const uint32_t ph = (t >> 1) & 1;
+    const bool ok = mbar_wait(&sb.k_empty[t & 1], ph, status) && mbar_wait(&sb.v_empty[t & 1], ph, status);
+    if (!__all_sync(FULL, ok)) return;
   }
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+    if (u.n[s] > 0 && !__all_sync(FULL, mbar_wait(&sb.o_done[s], 0, status))) return;
 }
 
 // ----------------------------------------------------------------- softmax / correction / epilogue
@@ -213,54 +267,54 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 template <int D, bool BF16>
-__device__ __forceinline__ void softmax_role(SmemBarriers<D>& sb, uint32_t tmem, const FwdParams& p, int q_tile,
-                                             int n_kv, int L, int tok0, int b, int h) {
+__device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, const FwdParams& p, const Unit u,
+                                             int s) {
   using C = TileCfg<D>;
   constexpr uint32_t FULL = 0xffffffffu;
-  const int t = threadIdx.x;  // query row inside the tile = tensor-memory lane
-  const uint32_t lane_off = (uint32_t)((t >> 5) * 32) << 16;
-  const int row_pos = q_tile * C::BM + t;  // logical position inside the sequence
+  const int n = s ? u.n[1] : u.n[0];
+  if (n == 0) return;
+  const int t = threadIdx.x & 127;  // query row inside the sub-tile = tensor-memory lane
+  const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = tmem + C::TM_S + s * 128 + lane_off;
+  const uint32_t tO = tmem + C::TM_O + s * 128 + lane_off;
+  const int row_pos = u.row0 + s * C::BM + t;  // logical position inside the sequence
   const float c2 = p.scale_log2;
   int* status = p.status;
   // Last eligible key position of this row: the diagonal under the causal
   // mask, and never past the end of the sequence.
-  const int last_key = p.causal ? min(row_pos, L - 1) : L - 1;
+  const int last_key = p.causal ? min(row_pos, u.L - 1) : u.L - 1;
   float m_run = -INFINITY;  // running maximum of the raw scores (scale > 0)
   float l_run = 0.f;        // sum of exp2(c2 * (s - m_run)) over the keys seen
 
-  for (int j = 0; j < n_kv; ++j) {
-    const int st = j & 1;
-    if (!__all_sync(FULL, mbar_wait(&sb.s_full[st], (j >> 1) & 1, status))) return;
+  for (int j = 0; j < n; ++j) {
+    if (!__all_sync(FULL, mbar_wait(&sb.s_full[s], j & 1, status))) return;
     tc_fence_after();
     uint32_t sr[C::BN];
-    const uint32_t s_addr = tmem + C::TM_S0 + st * 128 + lane_off;
-    tmem_ld_x32(s_addr + 0, sr + 0);
-    tmem_ld_x32(s_addr + 32, sr + 32);
-    tmem_ld_x32(s_addr + 64, sr + 64);
-    tmem_ld_x32(s_addr + 96, sr + 96);
+    tmem_ld_x32(tS + 0, sr + 0);
+    tmem_ld_x32(tS + 32, sr + 32);
+    tmem_ld_x32(tS + 64, sr + 64);
+    tmem_ld_x32(tS + 96, sr + 96);
     tmem_ld_wait32(sr);
     fence_regs32(sr + 32);
     fence_regs32(sr + 64);
     fence_regs32(sr + 96);
-    tc_fence_before();
-    mbar_arrive(&sb.s_empty[st]);  // S buffer may be overwritten by S_{j+2}
 
-    float s[C::BN];
+    float sv[C::BN];
 #pragma unroll
-    for (int i = 0; i < C::BN; ++i) s[i] = __uint_as_float(sr[i]);
+    for (int i = 0; i < C::BN; ++i) sv[i] = __uint_as_float(sr[i]);
     // Mask keys past the diagonal (causal) or past the sequence end.
     const int lim = last_key - j * C::BN;
     if (lim < C::BN - 1) {
 #pragma unroll
-      for (int i = 0; i < C::BN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+      for (int i = 0; i < C::BN; ++i) sv[i] = (i > lim) ? -INFINITY : sv[i];
     }
-    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+    float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
     for (int i = 4; i < C::BN; i += 4) {
-      mx0 = fmaxf(mx0, s[i]);
-      mx1 = fmaxf(mx1, s[i + 1]);
-      mx2 = fmaxf(mx2, s[i + 2]);
-      mx3 = fmaxf(mx3, s[i + 3]);
+      mx0 = fmaxf(mx0, sv[i]);
+      mx1 = fmaxf(mx1, sv[i + 1]);
+      mx2 = fmaxf(mx2, sv[i + 2]);
+      mx3 = fmaxf(mx3, sv[i + 3]);
     }
     const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
     const float m_new = fmaxf(m_run, m_tile);
@@ -277,55 +331,45 @@ __device__ __forceinline__ void softmax_role(SmemBarriers<D>& sb, uint32_t tmem,
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int i = 0; i < C::BN / 2; ++i) {
-      const float p0 = ex2_approx(fmaf(s[2 * i], c2, neg_mc));
-      const float p1 = ex2_approx(fmaf(s[2 * i + 1], c2, neg_mc));
+      const float p0 = ex2_approx(fmaf(sv[2 * i], c2, neg_mc));
+      const float p1 = ex2_approx(fmaf(sv[2 * i + 1], c2, neg_mc));
       rs0 += p0;
       rs1 += p1;
       pk[i] = pack2<BF16>(p0, p1);
     }
     l_run = l_run * alpha + (rs0 + rs1);
 
-    // P buffer st was last read by PV_{j-2}.
-    if (j >= 2) {
-      if (!__all_sync(FULL, mbar_wait(&sb.pv_done[st], ((j - 2) >> 1) & 1, status))) return;
-      tc_fence_after();
-    }
-    const uint32_t p_addr = tmem + C::TM_P0 + st * 64 + lane_off;
-    tmem_st_x32(p_addr, pk);
-    tmem_st_x32(p_addr + 32, pk + 32);
-
-    // Correction: O_acc *= alpha for rows whose maximum moved, after PV_{j-1}
-    // has landed and before PV_j is issued.
+    // Correction: O_s *= alpha for rows whose maximum moved.  PV_s(j-1) has
+    // completed: the commit that signalled S_s(j) covers it.
     if (j > 0 && __any_sync(FULL, rescale)) {
-      if (!__all_sync(FULL, mbar_wait(&sb.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, status))) return;
-      tc_fence_after();
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
-        tmem_ld_x32(tmem + C::TM_O + lane_off + c, o);
+        tmem_ld_x32(tO + c, o);
         tmem_ld_wait32(o);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st_x32(tmem + C::TM_O + lane_off + c, o);
+        tmem_st_x32(tO + c, o);
       }
     }
+    tmem_st_x32(tS, pk);  // P_s(j) over the first 64 cells of S_s(j)
+    tmem_st_x32(tS + 32, pk + 32);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&sb.p_full[st]);
+    mbar_arrive(&sb.p_full[s]);
   }
 
   // Epilogue: O = O_acc / l in the input type, lse = scale * m + ln l.
-  const int last = n_kv - 1;
-  if (!__all_sync(FULL, mbar_wait(&sb.pv_done[last & 1], (last >> 1) & 1, status))) return;
+  if (!__all_sync(FULL, mbar_wait(&sb.o_done[s], 0, status))) return;
   tc_fence_after();
-  const bool valid = row_pos < L;
+  const bool valid = row_pos < u.L;
   const float inv_l = 1.f / l_run;
   uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                  2 * ((int64_t)b * p.o_sb + (int64_t)h * p.o_sh + (int64_t)(tok0 + row_pos) * p.o_sn);
+                  2 * ((int64_t)u.b * p.o_sb + (int64_t)u.h * p.o_sh + (int64_t)(u.tok0 + row_pos) * p.o_sn);
 #pragma unroll
   for (int c = 0; c < D; c += 32) {
     uint32_t o[32];
-    tmem_ld_x32(tmem + C::TM_O + lane_off + c, o);
+    tmem_ld_x32(tO + c, o);
     tmem_ld_wait32(o);
     uint32_t w[16];
 #pragma unroll
@@ -340,37 +384,51 @@ __device__ __forceinline__ void softmax_role(SmemBarriers<D>& sb, uint32_t tmem,
     }
   }
   if (valid && p.lse != nullptr)
-    p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + tok0 + row_pos] = m_run * p.scale + __logf(l_run);
+    p.lse[(int64_t)u.b * p.lse_sb + (int64_t)u.h * p.lse_sh + u.tok0 + row_pos] = m_run * p.scale + __logf(l_run);
 }
 
 // ----------------------------------------------------------------- kernel
-// Grid: x = (batch or sequence) * Hq + head, y = query tile counted from the
-// last one, so that the longest causal rows are dispatched first.
+// Grid: x = (batch or sequence) * Hq + head, y = 256-row query block counted
+// from the last one, so that the longest causal rows are dispatched first.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = TileCfg<D>;
-  __shared__ SmemBarriers<D> sb;
+  __shared__ SmemBarriers sb;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+  Unit u;
   const int bh = blockIdx.x;
-  const int h = bh % p.Hq, b = bh / p.Hq;
-  const int q_tile = (int)gridDim.y - 1 - (int)blockIdx.y;
-  int L = p.N, tok0 = 0, bcoord = b;
+  u.h = bh % p.Hq;
+  u.b = bh / p.Hq;
+  u.hk = u.h / p.group;
+  u.L = p.N;
+  u.tok0 = 0;
+  u.bcoord = u.b;
   if (p.cu_seqlens != nullptr) {
-    const int s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
+    const int s0 = p.cu_seqlens[u.b], s1 = p.cu_seqlens[u.b + 1];
     if (s0 < 0 || s1 < s0 || s1 > p.total_tokens || s1 - s0 > p.max_seqlen) {
       if (threadIdx.x == 0) atomicCAS(p.status, 0, (int)kDevBadSeqlens);
       return;
     }
-    L = s1 - s0;
-    tok0 = s0;
-    bcoord = 0;
+    u.L = s1 - s0;
+    u.tok0 = s0;
+    u.bcoord = 0;
   }
-  if (q_tile * C::BM >= L) return;  // uniform across the CTA
-  const int n_kv = p.causal ? q_tile + 1 : (L + C::BN - 1) / C::BN;
+  const int block = (int)gridDim.y - 1 - (int)blockIdx.y;
+  u.row0 = block * C::BLOCK_M;
+  if (u.row0 >= u.L) return;  // uniform across the CTA
+  const int n_all = (u.L + C::BN - 1) / C::BN;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int first = u.row0 + s * C::BM;
+    u.n[s] = first >= u.L ? 0 : (p.causal ? first / C::BN + 1 : n_all);
+  }
+  // (u.n is only ever indexed with compile-time or select-resolved indices,
+  // so it stays in registers.)
+  u.n_max = max(u.n[0], u.n[1]);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -382,18 +440,17 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&sb.v_full[i], 1);
       mbar_init(&sb.v_empty[i], 1);
       mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.s_empty[i], 128);
       mbar_init(&sb.p_full[i], 128);
-      mbar_init(&sb.pv_done[i], 1);
+      mbar_init(&sb.o_done[i], 1);
     }
     fence_mbar_init();
   }
-  if (warp == 4 && (threadIdx.x & 31) == 0) {
+  if (warp == 8 && (threadIdx.x & 31) == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&sb.tmem_base, 512);
     tmem_relinquish();
   }
@@ -402,20 +459,23 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = sb.tmem_base;
 
-  if (warp < 4) {
-    softmax_role<D, BF16>(sb, tmem, p, q_tile, n_kv, L, tok0, b, h);
-  } else if (warp == 4) {
-    producer_role<D>(&tmQ, &tmK, &tmV, sb, smem, tok0 + q_tile * C::BM, tok0, h, h / p.group, bcoord, n_kv,
-                     p.hn_swapped, p.status);
+  if (warp < 8) {
+    regs_grow<C::SOFTMAX_REGS>();
+    softmax_role<D, BF16>(sb, tmem, p, u, warp >> 2);
   } else {
-    constexpr uint32_t ab = BF16 ? 1u : 0u;
-    constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
-    constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
-    mma_role<D>(sb, smem, tmem, n_kv, idesc_s, idesc_pv, p.status);
+    regs_shrink<C::CTRL_REGS>();
+    if (warp == 8) {
+      producer_role<D>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status);
+    } else if (warp == 9) {
+      constexpr uint32_t ab = BF16 ? 1u : 0u;
+      constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
+      constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
+      mma_role<D>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
