@@ -27,7 +27,8 @@ __device__ int g_status_word;
 
 namespace {
 
-constexpr int kMaxTokens = 65535 * 128;  // grid.y bound on query tiles
+constexpr int kMaxTokens = 1 << 30;      // token coordinates stay well inside int32
+constexpr int kMaxGridYZ = 65535;         // heads and batch/sequences map to grid y and z
 thread_local int t_last_cuda_error = 0;
 
 int fail_cuda(cudaError_t e) {
@@ -171,12 +172,13 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
 }
 
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                   const FwdParams& p, unsigned gx, unsigned gy, cudaStream_t s) {
+                   const FwdParams& p, unsigned gx, unsigned gy, unsigned gz, cudaStream_t s) {
   const bool bf = dtype == ETATTN_BF16;
+  const dim3 g(gx, gy, gz);
   switch (D) {
-    case 32: return bf ? launch_fwd_d32_1(q, k, v, p, gx, gy, s) : launch_fwd_d32_0(q, k, v, p, gx, gy, s);
-    case 64: return bf ? launch_fwd_d64_1(q, k, v, p, gx, gy, s) : launch_fwd_d64_0(q, k, v, p, gx, gy, s);
-    default: return bf ? launch_fwd_d128_1(q, k, v, p, gx, gy, s) : launch_fwd_d128_0(q, k, v, p, gx, gy, s);
+    case 32: return bf ? launch_fwd_d32_1(q, k, v, p, g, s) : launch_fwd_d32_0(q, k, v, p, g, s);
+    case 64: return bf ? launch_fwd_d64_1(q, k, v, p, g, s) : launch_fwd_d64_0(q, k, v, p, g, s);
+    default: return bf ? launch_fwd_d128_1(q, k, v, p, g, s) : launch_fwd_d128_0(q, k, v, p, g, s);
   }
 }
 
@@ -194,7 +196,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
              int dtype, const int64_t* strides, int causal, float scale, void* stream, bool do_launch) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (B < 0 || Hq < 0 || N < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
-  if (N > kMaxTokens || (int64_t)B * Hq > INT_MAX) return ETATTN_ERR_BAD_SHAPE;
+  if (N > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
@@ -245,8 +247,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  const unsigned gx = (unsigned)(B * Hq), gy = (unsigned)((N + 255) / 256);
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
+  const unsigned gx = (unsigned)((N + 255) / 256), gy = (unsigned)Hq, gz = (unsigned)B;
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, gz, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }
@@ -256,7 +258,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
                 int D, int dtype, const int64_t* strides, int causal, float scale, void* stream, bool do_launch) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (num_seqs < 0 || max_seqlen < 0 || total_tokens < 0 || Hq < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
-  if (max_seqlen > kMaxTokens || (int64_t)num_seqs * Hq > INT_MAX) return ETATTN_ERR_BAD_SHAPE;
+  if (max_seqlen > kMaxTokens || num_seqs > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
@@ -316,8 +318,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  const unsigned gx = (unsigned)(num_seqs * Hq), gy = (unsigned)((max_seqlen + 255) / 256);
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, static_cast<cudaStream_t>(stream));
+  const unsigned gx = (unsigned)((max_seqlen + 255) / 256), gy = (unsigned)Hq, gz = (unsigned)num_seqs;
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, gz, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }

@@ -22,7 +22,7 @@
 namespace etattn {
 
 cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
-                            unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
+                            dim3 grid, cudaStream_t stream) {
   using C = TileCfg<ETATTN_INST_D>;
   auto kern = attn_fwd_kernel<ETATTN_INST_D, ETATTN_INST_BF16 != 0>;
   // The dynamic shared-memory opt-in is per device; set it once per device.
@@ -42,7 +42,7 @@ cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CU
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<dim3(grid_x, grid_y, 1), C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
   return cudaGetLastError();
 }
 

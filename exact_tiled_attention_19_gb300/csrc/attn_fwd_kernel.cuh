@@ -18,8 +18,8 @@
 //   warpgroup 0 (warps 0-3)  softmax + correction + epilogue of sub-tile 0:
 //                            thread t owns row t (tensor-memory lane t).
 //   warpgroup 1 (warps 4-7)  the same for sub-tile 1.
-//   warp 8                   TMA producer: Q0, Q1 once, then K_j, V_j into
-//                            two-stage rings.
+//   warp 8                   TMA producer: Q0, Q1 once, then K_j into a
+//                            three-stage ring and V_j into a two-stage ring.
 //   warp 9                   tensor-memory allocator and MMA issuer.
 //   warps 10-11              no work (they complete warpgroup 2).
 //
@@ -30,7 +30,7 @@
 //
 // MMA issue order per key tile j >= 1:
 //   PV_0(j-1), S_0(j), PV_1(j-1), S_1(j)
-// so the softmax of one sub-tile overlaps two MMAs of the other, and a
+// so the softmax of one sub-tile overlaps two MMA groups of the other, and a
 // commit on S_s(j) also covers PV_s(j-1) (a commit tracks every earlier
 // tcgen05 operation of the issuing thread): when the softmax of sub-tile s
 // sees S_s(j), O_s is up to date and may be rescaled.  S_s(j+1) overwrites
@@ -89,20 +89,21 @@ struct TileCfg {
   static constexpr int KSTEPS_PER_CHUNK = SW_ELEMS / 16;
   static constexpr int Q_BYTES = BM * D * 2;           // one sub-tile
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int STAGES = 2;
+  static constexpr int K_STAGES = 3;
+  static constexpr int V_STAGES = 2;
   static constexpr int OFF_Q = 0;                      // Q_0 then Q_1
   static constexpr int OFF_K = 2 * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int SMEM_BYTES = OFF_V + STAGES * KV_BYTES + 1024;  // + alignment slack
+  static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;
+  static constexpr int SMEM_BYTES = OFF_V + V_STAGES * KV_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t SBO = 8 * SW_BYTES;        // stride between 8-row swizzle atoms
-  static constexpr uint32_t TM_S = 0, TM_O = 256;      // + 128 * sub-tile
+  static constexpr uint32_t TM_S = 0, TM_O = 256;      // + 128 per sub-tile
   static constexpr int THREADS = 384;
   // Register split: 384 threads launch with LAUNCH_REGS each; warpgroup 2
   // (TMA + MMA) shrinks to CTRL_REGS so that the two softmax warpgroups can
   // grow to SOFTMAX_REGS.  128*CTRL_REGS + 256*SOFTMAX_REGS == 384*LAUNCH_REGS.
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = 56;
-  static constexpr int SOFTMAX_REGS = 224;
+  static constexpr int CTRL_REGS = 88;
+  static constexpr int SOFTMAX_REGS = 208;
   static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS, "register split over budget");
 };
 
@@ -112,7 +113,7 @@ __device__ __forceinline__ void fence_regs32(uint32_t* r) {
 
 struct SmemBarriers {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
+  uint64_t k_full[3], k_empty[3];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2];            // per sub-tile: S_s(j) is in tensor memory (and PV_s(j-1) is done)
   uint64_t p_full[2];            // per sub-tile: P_s(j) written and O_s corrected
@@ -126,19 +127,21 @@ struct Unit {
   int tok0;                      // first token of the sequence (packed batch), else 0
   int L;                         // sequence length
   int row0;                      // first query row (logical position) of sub-tile 0
-  int n[2];                      // key tiles visited by sub-tile 0 / 1 (0 = sub-tile idle)
+  int n0, n1;                    // key tiles visited by sub-tile 0 / 1 (0 = sub-tile idle)
+  __device__ __forceinline__ int n(int s) const { return s ? n1 : n0; }
   int n_max;
 };
 
 // ----------------------------------------------------------------- producer
+// Runs on one thread.  (Waits are single-thread too: 32 lanes polling one
+// mbarrier serialise on it and cost more than a tile's MMA issue slot.)
 template <int D>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, SmemBarriers& sb, uint8_t* smem,
                                               const Unit u, int hn_swapped, int* status) {
   using C = TileCfg<D>;
-  const int lane = threadIdx.x & 31;
   const bool swq = hn_swapped & 1, swk = (hn_swapped >> 1) & 1, swv = (hn_swapped >> 2) & 1;
-  if (lane == 0) {
+  {
     mbar_arrive_expect_tx(&sb.q_full, 2 * C::Q_BYTES);
 #pragma unroll
     for (int s = 0; s < 2; ++s)
@@ -147,43 +150,60 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
         tma_load_tile(smem + C::OFF_Q + s * C::Q_BYTES + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full,
                       c * C::SW_ELEMS, u.tok0 + u.row0 + s * C::BM, u.h, u.bcoord, swq);
   }
+  int ks = 0, kph = 0;  // K ring slot and its phase for tile j
   for (int j = 0; j < u.n_max; ++j) {
-    const int st = j & 1;
-    const uint32_t ph_prev = ((j - 2) >> 1) & 1;
-    if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sb.k_empty[st], ph_prev, status))) return;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&sb.k_full[st], C::KV_BYTES);
+    // K_j goes to slot j % 3, whose previous tile j-3 must have been released.
+    if (j >= C::K_STAGES && !mbar_wait(&sb.k_empty[ks], kph ^ 1, status)) return;
+    {
+      mbar_arrive_expect_tx(&sb.k_full[ks], C::KV_BYTES);
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
-        tma_load_tile(smem + C::OFF_K + st * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmK, &sb.k_full[st],
+        tma_load_tile(smem + C::OFF_K + ks * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmK, &sb.k_full[ks],
                       c * C::SW_ELEMS, u.tok0 + j * C::BN, u.hk, u.bcoord, swk);
     }
-    if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sb.v_empty[st], ph_prev, status))) return;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&sb.v_full[st], C::KV_BYTES);
+    if (++ks == C::K_STAGES) {
+      ks = 0;
+      kph ^= 1;
+    }
+    const int vs = j & 1;
+    if (j >= 2 && !mbar_wait(&sb.v_empty[vs], ((j - 2) >> 1) & 1, status)) return;
+    {
+      mbar_arrive_expect_tx(&sb.v_full[vs], C::KV_BYTES);
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
-        tma_load_tile(smem + C::OFF_V + st * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmV, &sb.v_full[st],
+        tma_load_tile(smem + C::OFF_V + vs * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmV, &sb.v_full[vs],
                       c * C::SW_ELEMS, u.tok0 + j * C::BN, u.hk, u.bcoord, swv);
     }
-    __syncwarp();
   }
 }
 
 // ----------------------------------------------------------------- MMA issuer
+// Descriptors are built once per CTA; every k-step then adds a compile-time
+// offset (in 16-byte units) to the 64-bit descriptor.  The 14-bit address
+// field cannot overflow: shared memory addresses stay below 2^18 bytes.
+// Keeping the issuing thread's work per MMA to an add and the instruction
+// itself is what lets the tensor core run at full rate (a descriptor rebuilt
+// per MMA costs more cycles than a 128x128x16 MMA takes).
+struct MmaDescs {
+  uint64_t q0, q1;      // Q_s, K-major
+  uint64_t k0, k1, k2;  // K slots, K-major
+  uint64_t v0, v1;      // V slots, MN-major
+};
+
 // S_s = Q_s K^T: both K-major (d contiguous); a 16-element step moves 32 bytes
 // inside a swizzled row, and a new d-chunk starts a new TMA box.
 template <int D>
-__device__ __forceinline__ void issue_s(uint8_t* smem, uint32_t tmem, int s, int st, uint32_t idesc) {
+__device__ __forceinline__ void issue_s(const MmaDescs& md, uint32_t tmem, int s, int ks, uint32_t idesc) {
   using C = TileCfg<D>;
-  const uint32_t q_base = smem_u32(smem + C::OFF_Q + s * C::Q_BYTES);
-  const uint32_t k_base = smem_u32(smem + C::OFF_K + st * C::KV_BYTES);
+  const uint64_t qd = s ? md.q1 : md.q0;
+  const uint64_t kd = ks == 0 ? md.k0 : (ks == 1 ? md.k1 : md.k2);
+  const uint32_t d_tmem = tmem + C::TM_S + s * 128;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const int c = kk / C::KSTEPS_PER_CHUNK, w = kk % C::KSTEPS_PER_CHUNK;
-    const uint64_t qdesc = smem_desc(q_base + c * C::BM * C::SW_BYTES + w * 32, 16, C::SBO, C::SWIZZLE);
-    const uint64_t kdesc = smem_desc(k_base + c * C::BN * C::SW_BYTES + w * 32, 16, C::SBO, C::SWIZZLE);
-    mma_ss(tmem + C::TM_S + s * 128, qdesc, kdesc, idesc, kk > 0 ? 1u : 0u);
+    const uint64_t qoff = (uint64_t)((c * C::BM * C::SW_BYTES + w * 32) >> 4);
+    const uint64_t koff = (uint64_t)((c * C::BN * C::SW_BYTES + w * 32) >> 4);
+    mma_ss(d_tmem, qd + qoff, kd + koff, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -191,76 +211,93 @@ __device__ __forceinline__ void issue_s(uint8_t* smem, uint32_t tmem, int s, int
 // B = V MN-major (d contiguous): 16 keys = 16 swizzled rows per step; LBO
 // steps between d-chunks, SBO between 8-row groups.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint8_t* smem, uint32_t tmem, int s, int st, bool accumulate,
+__device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int s, int st, bool accumulate,
                                          uint32_t idesc) {
   using C = TileCfg<D>;
-  const uint32_t v_base = smem_u32(smem + C::OFF_V + st * C::KV_BYTES);
+  const uint64_t vd = st ? md.v1 : md.v0;
   const uint32_t p_base = tmem + C::TM_S + s * 128;
+  const uint32_t d_tmem = tmem + C::TM_O + s * 128;
+  const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
-  for (int kk = 0; kk < C::BN / 16; ++kk) {
-    const uint64_t vdesc = smem_desc(v_base + kk * 16 * C::SW_BYTES, C::BN * C::SW_BYTES, C::SBO, C::SWIZZLE);
-    mma_ts(tmem + C::TM_O + s * 128, p_base + kk * 8, vdesc, idesc, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < C::BN / 16; ++kk)
+    mma_ts(d_tmem, p_base + kk * 8, vd + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), idesc, kk > 0 ? 1u : acc0);
 }
 
+// Runs on one thread: the tensor pipe queues only a couple of MMAs, so any
+// cycle the issuing thread spends elsewhere between groups is idle tensor time.
 template <int D>
 __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
-  constexpr uint32_t FULL = 0xffffffffu;
-  const bool leader = (threadIdx.x & 31) == 0;
-  if (!__all_sync(FULL, mbar_wait(&sb.q_full, 0, status) && mbar_wait(&sb.k_full[0], 0, status))) return;
+  using C = TileCfg<D>;
+  MmaDescs md;
+  md.q0 = smem_desc(smem_u32(smem + C::OFF_Q), 16, C::SBO, C::SWIZZLE);
+  md.q1 = md.q0 + (uint64_t)(C::Q_BYTES >> 4);
+  md.k0 = smem_desc(smem_u32(smem + C::OFF_K), 16, C::SBO, C::SWIZZLE);
+  md.k1 = md.k0 + (uint64_t)(C::KV_BYTES >> 4);
+  md.k2 = md.k1 + (uint64_t)(C::KV_BYTES >> 4);
+  md.v0 = smem_desc(smem_u32(smem + C::OFF_V), C::BN * C::SW_BYTES, C::SBO, C::SWIZZLE);
+  md.v1 = md.v0 + (uint64_t)(C::KV_BYTES >> 4);
+  if (!mbar_wait(&sb.q_full, 0, status)) return;
+
+  int ks = 0, kph = 0;  // K ring slot / phase of the next key tile
+  if (!mbar_wait(&sb.k_full[0], 0, status)) return;
   tc_fence_after();
-  if (leader) {
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      if (u.n[s] > 0) {
-        issue_s<D>(smem, tmem, s, 0, idesc_s);
-        mma_commit(&sb.s_full[s]);
-      }
+  for (int sub = 0; sub < 2; ++sub) {
+    if (u.n(sub) > 0) {
+      issue_s<D>(md, tmem, sub, 0, idesc_s);
+      mma_commit(&sb.s_full[sub]);
     }
-    mma_commit(&sb.k_empty[0]);
   }
-  __syncwarp();
+  mma_commit(&sb.k_empty[0]);
+  ks = 1;
   for (int j = 1; j <= u.n_max; ++j) {
     const int i = j - 1;  // key tile whose PV products are issued in this step
     const bool has_k = j < u.n_max;
-    bool ok = mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status);
-    if (has_k) ok = ok && mbar_wait(&sb.k_full[j & 1], (j >> 1) & 1, status);
-    if (!__all_sync(FULL, ok)) return;
+    if (has_k && !mbar_wait(&sb.k_full[ks], kph, status)) return;
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      if (i < u.n[s]) {
-        if (!__all_sync(FULL, mbar_wait(&sb.p_full[s], i & 1, status))) return;
+    for (int sub = 0; sub < 2; ++sub) {
+      if (i < u.n(sub)) {  // PV_sub(i)
+        if (!mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.p_full[sub], i & 1, status)) return;
         tc_fence_after();
-        if (leader) {
-          issue_pv<D>(smem, tmem, s, i & 1, i > 0, idesc_pv);
-          if (i == u.n[s] - 1) mma_commit(&sb.o_done[s]);
-        }
+        issue_pv<D>(md, tmem, sub, i & 1, i > 0, idesc_pv);
+        if (i == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
       }
-      if (s == 1 && leader) mma_commit(&sb.v_empty[i & 1]);  // both PV products of tile i issued
-      if (j < u.n[s] && leader) {
-        issue_s<D>(smem, tmem, s, j & 1, idesc_s);
-        mma_commit(&sb.s_full[s]);
+      if (sub == 1) mma_commit(&sb.v_empty[i & 1]);  // every PV product of tile i is issued
+      if (j < u.n(sub)) {  // S_sub(j)
+        issue_s<D>(md, tmem, sub, ks, idesc_s);
+        mma_commit(&sb.s_full[sub]);
       }
-      __syncwarp();
     }
-    if (has_k && leader) mma_commit(&sb.k_empty[j & 1]);
-    __syncwarp();
+    if (has_k) {
+      mma_commit(&sb.k_empty[ks]);
+      if (++ks == C::K_STAGES) {
+        ks = 0;
+        kph ^= 1;
+      }
+    }
   }
-  // Drain: wait for the commit arrivals nobody else consumes (the last two
-  // tiles' stage releases, and the final PV of an idle-epilogue sub-tile) so
-  // that no arrival can land in shared memory after the CTA exits.
-  for (int t = u.n_max >= 2 ? u.n_max - 2 : 0; t < u.n_max; ++t) {
-    const uint32_t ph = (t >> 1) & 1;
-    const bool ok = mbar_wait(&sb.k_empty[t & 1], ph, status) && mbar_wait(&sb.v_empty[t & 1], ph, status);
-    if (!__all_sync(FULL, ok)) return;
-  }
+  // Drain: wait for the commit arrivals nobody else consumes (the last
+  // tiles' ring releases and the final PV of each sub-tile) so that no
+  // arrival can land in shared memory after the CTA exits.
+  for (int t = u.n_max > C::K_STAGES ? u.n_max - C::K_STAGES : 0; t < u.n_max; ++t)
+    if (!mbar_wait(&sb.k_empty[t % C::K_STAGES], (t / C::K_STAGES) & 1, status)) return;
+  for (int t = u.n_max >= 2 ? u.n_max - 2 : 0; t < u.n_max; ++t)
+    if (!mbar_wait(&sb.v_empty[t & 1], (t >> 1) & 1, status)) return;
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
-    if (u.n[s] > 0 && !__all_sync(FULL, mbar_wait(&sb.o_done[s], 0, status))) return;
+  for (int sub = 0; sub < 2; ++sub)
+    if (u.n(sub) > 0 && !mbar_wait(&sb.o_done[sub], 0, status)) return;
 }
 
 // ----------------------------------------------------------------- softmax / correction / epilogue
+// Warp-wide wait: lane 0 polls the barrier and the outcome is broadcast, so
+// one thread per warp (not 32) touches the barrier word.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
@@ -271,7 +308,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
                                              int s) {
   using C = TileCfg<D>;
   constexpr uint32_t FULL = 0xffffffffu;
-  const int n = s ? u.n[1] : u.n[0];
+  const int n = s ? u.n1 : u.n0;
   if (n == 0) return;
   const int t = threadIdx.x & 127;  // query row inside the sub-tile = tensor-memory lane
   const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
@@ -287,34 +324,43 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   float l_run = 0.f;        // sum of exp2(c2 * (s - m_run)) over the keys seen
 
   for (int j = 0; j < n; ++j) {
-    if (!__all_sync(FULL, mbar_wait(&sb.s_full[s], j & 1, status))) return;
+    if (!warp_wait(&sb.s_full[s], j & 1, status)) return;
     tc_fence_after();
+    // Scores arrive in two halves: the maximum of the first half is taken
+    // while the second half is still being read from tensor memory.
     uint32_t sr[C::BN];
     tmem_ld_x32(tS + 0, sr + 0);
     tmem_ld_x32(tS + 32, sr + 32);
-    tmem_ld_x32(tS + 64, sr + 64);
-    tmem_ld_x32(tS + 96, sr + 96);
     tmem_ld_wait32(sr);
     fence_regs32(sr + 32);
-    fence_regs32(sr + 64);
-    fence_regs32(sr + 96);
+    tmem_ld_x32(tS + 64, sr + 64);
+    tmem_ld_x32(tS + 96, sr + 96);
 
     float sv[C::BN];
-#pragma unroll
-    for (int i = 0; i < C::BN; ++i) sv[i] = __uint_as_float(sr[i]);
     // Mask keys past the diagonal (causal) or past the sequence end.
     const int lim = last_key - j * C::BN;
-    if (lim < C::BN - 1) {
+    const bool masked = lim < C::BN - 1;
 #pragma unroll
-      for (int i = 0; i < C::BN; ++i) sv[i] = (i > lim) ? -INFINITY : sv[i];
+    for (int i = 0; i < C::BN / 2; ++i) sv[i] = (masked && i > lim) ? -INFINITY : __uint_as_float(sr[i]);
+    float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
+    float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
+#pragma unroll
+    for (int i = 8; i < C::BN / 2; i += 8) {
+      mx0 = max3(mx0, sv[i], sv[i + 1]);
+      mx1 = max3(mx1, sv[i + 2], sv[i + 3]);
+      mx2 = max3(mx2, sv[i + 4], sv[i + 5]);
+      mx3 = max3(mx3, sv[i + 6], sv[i + 7]);
     }
-    float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+    tmem_ld_wait32(sr + 64);
+    fence_regs32(sr + 96);
 #pragma unroll
-    for (int i = 4; i < C::BN; i += 4) {
-      mx0 = fmaxf(mx0, sv[i]);
-      mx1 = fmaxf(mx1, sv[i + 1]);
-      mx2 = fmaxf(mx2, sv[i + 2]);
-      mx3 = fmaxf(mx3, sv[i + 3]);
+    for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = (masked && i > lim) ? -INFINITY : __uint_as_float(sr[i]);
+#pragma unroll
+    for (int i = C::BN / 2; i < C::BN; i += 8) {
+      mx0 = max3(mx0, sv[i], sv[i + 1]);
+      mx1 = max3(mx1, sv[i + 2], sv[i + 3]);
+      mx2 = max3(mx2, sv[i + 4], sv[i + 5]);
+      mx3 = max3(mx3, sv[i + 6], sv[i + 7]);
     }
     const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
     const float m_new = fmaxf(m_run, m_tile);
@@ -327,16 +373,26 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
       m_run = m_new;
     }
     const float neg_mc = -m_run * c2;
+    // p = exp2(s * c2 - m * c2): the scaling runs two lanes per instruction,
+    // the row sum in four independent pairs of accumulators.
     uint32_t pk[C::BN / 2];
-    float rs0 = 0.f, rs1 = 0.f;
+    float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f, rc0 = 0.f, rc1 = 0.f, rd0 = 0.f, rd1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < C::BN / 2; ++i) {
-      const float p0 = ex2_approx(fmaf(sv[2 * i], c2, neg_mc));
-      const float p1 = ex2_approx(fmaf(sv[2 * i + 1], c2, neg_mc));
-      rs0 += p0;
-      rs1 += p1;
-      pk[i] = pack2<BF16>(p0, p1);
+    for (int i = 0; i < C::BN / 2; i += 4) {
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
+      add2(ra0, ra1, x[0], x[1]);
+      add2(rb0, rb1, x[2], x[3]);
+      add2(rc0, rc1, x[4], x[5]);
+      add2(rd0, rd1, x[6], x[7]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
     }
+    const float rs0 = (ra0 + rb0) + (rc0 + rd0), rs1 = (ra1 + rb1) + (rc1 + rd1);
     l_run = l_run * alpha + (rs0 + rs1);
 
     // Correction: O_s *= alpha for rows whose maximum moved.  PV_s(j-1) has
@@ -360,7 +416,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   }
 
   // Epilogue: O = O_acc / l in the input type, lse = scale * m + ln l.
-  if (!__all_sync(FULL, mbar_wait(&sb.o_done[s], 0, status))) return;
+  if (!warp_wait(&sb.o_done[s], 0, status)) return;
   tc_fence_after();
   const bool valid = row_pos < u.L;
   const float inv_l = 1.f / l_run;
@@ -388,8 +444,10 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 }
 
 // ----------------------------------------------------------------- kernel
-// Grid: x = (batch or sequence) * Hq + head, y = 256-row query block counted
-// from the last one, so that the longest causal rows are dispatched first.
+// Grid: x = 256-row query block counted from the last one, y = query head,
+// z = batch (or sequence).  CTAs are dispatched in that order, so the CTAs
+// running at any time mostly belong to a few heads and share their K/V tiles
+// in L2, and within a head the longest causal rows start first.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -400,9 +458,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   Unit u;
-  const int bh = blockIdx.x;
-  u.h = bh % p.Hq;
-  u.b = bh / p.Hq;
+  u.h = blockIdx.y;
+  u.b = blockIdx.z;
   u.hk = u.h / p.group;
   u.L = p.N;
   u.tok0 = 0;
@@ -417,32 +474,34 @@ __global__ void __launch_bounds__(384, 1)
     u.tok0 = s0;
     u.bcoord = 0;
   }
-  const int block = (int)gridDim.y - 1 - (int)blockIdx.y;
+  const int block = (int)gridDim.x - 1 - (int)blockIdx.x;
   u.row0 = block * C::BLOCK_M;
   if (u.row0 >= u.L) return;  // uniform across the CTA
   const int n_all = (u.L + C::BN - 1) / C::BN;
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int first = u.row0 + s * C::BM;
-    u.n[s] = first >= u.L ? 0 : (p.causal ? first / C::BN + 1 : n_all);
+  {
+    const int first1 = u.row0 + C::BM;
+    u.n0 = p.causal ? u.row0 / C::BN + 1 : n_all;  // row0 < L here
+    u.n1 = first1 >= u.L ? 0 : (p.causal ? first1 / C::BN + 1 : n_all);
   }
-  // (u.n is only ever indexed with compile-time or select-resolved indices,
-  // so it stays in registers.)
-  u.n_max = max(u.n[0], u.n[1]);
+  u.n_max = max(u.n0, u.n1);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
     mbar_init(&sb.q_full, 1);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::K_STAGES; ++i) {
       mbar_init(&sb.k_full[i], 1);
       mbar_init(&sb.k_empty[i], 1);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.v_full[i], 1);
       mbar_init(&sb.v_empty[i], 1);
       mbar_init(&sb.s_full[i], 1);
       mbar_init(&sb.p_full[i], 128);
       mbar_init(&sb.o_done[i], 1);
     }
+
     fence_mbar_init();
   }
   if (warp == 8 && (threadIdx.x & 31) == 0) {
@@ -464,13 +523,16 @@ __global__ void __launch_bounds__(384, 1)
     softmax_role<D, BF16>(sb, tmem, p, u, warp >> 2);
   } else {
     regs_shrink<C::CTRL_REGS>();
+    const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp == 8) {
-      producer_role<D>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status);
+      if (lane0) producer_role<D>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status);
+      __syncwarp();
     } else if (warp == 9) {
       constexpr uint32_t ab = BF16 ? 1u : 0u;
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
-      mma_role<D>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+      if (lane0) mma_role<D>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+      __syncwarp();
     }
   }
   tc_fence_before();

@@ -65,7 +65,8 @@ def test_status_strings_and_version():
 
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=2), 2),
-    (dict(D=96), 3), (dict(D=256), 3), (dict(N=-1), 3), (dict(B=-1), 3), (dict(N=65535 * 128 + 1), 3),
+    (dict(D=96), 3), (dict(D=256), 3), (dict(N=-1), 3), (dict(B=-1), 3), (dict(N=2 ** 30 + 1), 3),
+    (dict(B=65536), 3), (dict(Hq=65536, Hkv=1), 3),
     (dict(Hkv=0), 4), (dict(Hkv=3), 4), (dict(Hq=4, Hkv=8), 4),
     (dict(scale=0.0), 8), (dict(scale=-1.0), 8), (dict(scale=float("inf")), 8), (dict(scale=float("nan")), 8),
     (dict(q=0), 1), (dict(o=0), 1), (dict(k=0), 1),

@@ -188,3 +188,16 @@ def test_host_buffer_entry_points_match_device_path():
     assert rc == 0
     s.synchronize()
     assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_repeated_calls_bit_identical_many_ctas(causal):
+    """Many CTAs, repeated calls on the same inputs: results are bit-identical
+    (catches reads of unwritten registers, tensor memory or shared memory)."""
+    inp = W.random_qkv(2, 16, 16, 640, 128, torch.bfloat16, seed=18)
+    dev = {n: t.cuda() for n, t in inp.items()}
+    o_ref, l_ref = binding.attention(dev["q"], dev["k"], dev["v"], causal=causal)
+    for _ in range(8):
+        o, l = binding.attention(dev["q"], dev["k"], dev["v"], causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
