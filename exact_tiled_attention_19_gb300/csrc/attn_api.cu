@@ -99,12 +99,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct DeviceInfo {
   std::atomic<int> state{0};  // 0 unknown, 1 ok, 2 unsupported
   int* status_word = nullptr;
+  int num_sms = 0;
 };
 DeviceInfo g_devices[64];
 std::mutex g_device_mu;
 
 // Current device, checked to be sm_103, with its status-word address.
-int current_device(int* dev_out, int** status_out) {
+int current_device(int* dev_out, int** status_out, int* num_sms_out = nullptr) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
@@ -124,6 +125,10 @@ int current_device(int* dev_out, int** status_out) {
       if (major != 10 || minor != 3) {
         d.state.store(2);
       } else {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+          cudaGetLastError();
+          return ETATTN_ERR_NO_DEVICE;
+        }
         void* sym = nullptr;
         cudaError_t se = cudaGetSymbolAddress(&sym, g_status_word);
         if (se != cudaSuccess) return fail_cuda(se);
@@ -135,6 +140,7 @@ int current_device(int* dev_out, int** status_out) {
   if (d.state.load() != 1) return ETATTN_ERR_NO_DEVICE;
   *dev_out = dev;
   *status_out = d.status_word;
+  if (num_sms_out) *num_sms_out = d.num_sms;
   return ETATTN_OK;
 }
 
@@ -171,14 +177,20 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
   return ETATTN_OK;
 }
 
+// Launch over `tokens` query rows per (head, batch/sequence).  Two 128-row
+// sub-tiles per CTA keep the tensor core busier, but halve the CTA count; a
+// problem that would not fill the GPU with two-sub-tile CTAs runs one
+// sub-tile per CTA instead.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                   const FwdParams& p, unsigned gx, unsigned gy, unsigned gz, cudaStream_t s) {
+                   const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, cudaStream_t s) {
   const bool bf = dtype == ETATTN_BF16;
-  const dim3 g(gx, gy, gz);
+  const int64_t blocks2 = (tokens + 255) / 256;
+  const int nsub = blocks2 * (int64_t)gy * gz < num_sms ? 1 : 2;
+  const dim3 g((unsigned)(nsub == 2 ? blocks2 : (tokens + 127) / 128), gy, gz);
   switch (D) {
-    case 32: return bf ? launch_fwd_d32_1(q, k, v, p, g, s) : launch_fwd_d32_0(q, k, v, p, g, s);
-    case 64: return bf ? launch_fwd_d64_1(q, k, v, p, g, s) : launch_fwd_d64_0(q, k, v, p, g, s);
-    default: return bf ? launch_fwd_d128_1(q, k, v, p, g, s) : launch_fwd_d128_0(q, k, v, p, g, s);
+    case 32: return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, s) : launch_fwd_d32_0(q, k, v, p, g, nsub, s);
+    case 64: return bf ? launch_fwd_d64_1(q, k, v, p, g, nsub, s) : launch_fwd_d64_0(q, k, v, p, g, nsub, s);
+    default: return bf ? launch_fwd_d128_1(q, k, v, p, g, nsub, s) : launch_fwd_d128_0(q, k, v, p, g, nsub, s);
   }
 }
 
@@ -220,7 +232,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
   int dev = 0;
   int* status = nullptr;
-  if (int rc = current_device(&dev, &status)) return rc;
+  int num_sms = 0;
+  if (int rc = current_device(&dev, &status, &num_sms)) return rc;
 
   CUtensorMap mq, mk, mv;
   bool swq = false, swk = false, swv = false;
@@ -247,8 +260,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  const unsigned gx = (unsigned)((N + 255) / 256), gy = (unsigned)Hq, gz = (unsigned)B;
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, gz, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, N, (unsigned)Hq, (unsigned)B, num_sms,
+                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }
@@ -291,7 +304,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
   int dev = 0;
   int* status = nullptr;
-  if (int rc = current_device(&dev, &status)) return rc;
+  int num_sms = 0;
+  if (int rc = current_device(&dev, &status, &num_sms)) return rc;
 
   CUtensorMap mq, mk, mv;
   bool swq = false, swk = false, swv = false;
@@ -318,8 +332,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  const unsigned gx = (unsigned)((max_seqlen + 255) / 256), gy = (unsigned)Hq, gz = (unsigned)num_seqs;
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, gx, gy, gz, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, max_seqlen, (unsigned)Hq, (unsigned)num_seqs, num_sms,
+                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }

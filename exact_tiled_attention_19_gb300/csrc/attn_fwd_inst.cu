@@ -21,10 +21,13 @@
 
 namespace etattn {
 
-cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
-                            dim3 grid, cudaStream_t stream) {
-  using C = TileCfg<ETATTN_INST_D>;
-  auto kern = attn_fwd_kernel<ETATTN_INST_D, ETATTN_INST_BF16 != 0>;
+namespace {
+
+template <int NSUB>
+cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p, dim3 grid,
+                       cudaStream_t stream) {
+  using C = TileCfg<ETATTN_INST_D, NSUB>;
+  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0>;
   // The dynamic shared-memory opt-in is per device; set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -32,18 +35,28 @@ cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CU
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
-    // The kernel re-splits its registers between warpgroups (setmaxnreg); the
-    // split is only valid if every thread launches with LAUNCH_REGS registers.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    if (NSUB == 2) {
+      // The two-sub-tile kernel re-splits its registers between warpgroups
+      // (setmaxnreg); the split is only valid if every thread launches with
+      // LAUNCH_REGS registers.
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
+                            dim3 grid, int nsub, cudaStream_t stream) {
+  return nsub == 1 ? launch_one<1>(q, k, v, p, grid, stream) : launch_one<2>(q, k, v, p, grid, stream);
 }
 
 }  // namespace etattn

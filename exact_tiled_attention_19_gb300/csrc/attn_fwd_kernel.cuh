@@ -77,10 +77,11 @@ __device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map,
     tma_load_4d(dst, map, bar, d0, row, head, batch);
 }
 
-template <int D>
+template <int D, int NSUB_>
 struct TileCfg {
+  static constexpr int NSUB = NSUB_;                   // 128-row query sub-tiles per CTA (1 or 2)
   static constexpr int BM = 128;                       // query rows per sub-tile
-  static constexpr int BLOCK_M = 2 * BM;               // query rows per CTA
+  static constexpr int BLOCK_M = NSUB * BM;            // query rows per CTA
   static constexpr int BN = 128;                       // keys per tile
   static constexpr int SW_ELEMS = D >= 64 ? 64 : 32;   // elements per swizzled smem row
   static constexpr int SW_BYTES = SW_ELEMS * 2;        // 128 B (D >= 64) or 64 B (D = 32)
@@ -91,20 +92,25 @@ struct TileCfg {
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int K_STAGES = 3;
   static constexpr int V_STAGES = 2;
-  static constexpr int OFF_Q = 0;                      // Q_0 then Q_1
-  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_Q = 0;                      // Q_0 (then Q_1)
+  static constexpr int OFF_K = NSUB * Q_BYTES;
   static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;
   static constexpr int SMEM_BYTES = OFF_V + V_STAGES * KV_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t SBO = 8 * SW_BYTES;        // stride between 8-row swizzle atoms
-  static constexpr uint32_t TM_S = 0, TM_O = 256;      // + 128 per sub-tile
-  static constexpr int THREADS = 384;
+  static constexpr uint32_t TM_S = 0, TM_O = NSUB * 128;  // + 128 per sub-tile
+  static constexpr uint32_t TMEM_COLS = NSUB * 256;
+  // Warps: 4 softmax warps per sub-tile, then the TMA warp and the MMA warp,
+  // padded to whole warpgroups.
+  static constexpr int PRODUCER_WARP = 4 * NSUB, MMA_WARP = 4 * NSUB + 1;
+  static constexpr int THREADS = NSUB == 2 ? 384 : 256;
   // Register split: 384 threads launch with LAUNCH_REGS each; warpgroup 2
   // (TMA + MMA) shrinks to CTRL_REGS so that the two softmax warpgroups can
   // grow to SOFTMAX_REGS.  128*CTRL_REGS + 256*SOFTMAX_REGS == 384*LAUNCH_REGS.
   static constexpr int LAUNCH_REGS = 168;
   static constexpr int CTRL_REGS = 88;
   static constexpr int SOFTMAX_REGS = 208;
-  static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS, "register split over budget");
+  static_assert(NSUB == 1 || 128 * CTRL_REGS + 256 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
+                "register split over budget");
 };
 
 __device__ __forceinline__ void fence_regs32(uint32_t* r) {
@@ -135,16 +141,16 @@ struct Unit {
 // ----------------------------------------------------------------- producer
 // Runs on one thread.  (Waits are single-thread too: 32 lanes polling one
 // mbarrier serialise on it and cost more than a tile's MMA issue slot.)
-template <int D>
+template <int D, int NSUB>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, SmemBarriers& sb, uint8_t* smem,
                                               const Unit u, int hn_swapped, int* status) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, NSUB>;
   const bool swq = hn_swapped & 1, swk = (hn_swapped >> 1) & 1, swv = (hn_swapped >> 2) & 1;
   {
-    mbar_arrive_expect_tx(&sb.q_full, 2 * C::Q_BYTES);
+    mbar_arrive_expect_tx(&sb.q_full, NSUB * C::Q_BYTES);
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
+    for (int s = 0; s < NSUB; ++s)
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_Q + s * C::Q_BYTES + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full,
@@ -192,9 +198,9 @@ struct MmaDescs {
 
 // S_s = Q_s K^T: both K-major (d contiguous); a 16-element step moves 32 bytes
 // inside a swizzled row, and a new d-chunk starts a new TMA box.
-template <int D>
+template <int D, int NSUB>
 __device__ __forceinline__ void issue_s(const MmaDescs& md, uint32_t tmem, int s, int ks, uint32_t idesc) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, NSUB>;
   const uint64_t qd = s ? md.q1 : md.q0;
   const uint64_t kd = ks == 0 ? md.k0 : (ks == 1 ? md.k1 : md.k2);
   const uint32_t d_tmem = tmem + C::TM_S + s * 128;
@@ -210,10 +216,10 @@ __device__ __forceinline__ void issue_s(const MmaDescs& md, uint32_t tmem, int s
 // O_s (+)= P_s V: A = P_s from tensor memory (8 cells = 16 keys per step),
 // B = V MN-major (d contiguous): 16 keys = 16 swizzled rows per step; LBO
 // steps between d-chunks, SBO between 8-row groups.
-template <int D>
+template <int D, int NSUB>
 __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int s, int st, bool accumulate,
                                          uint32_t idesc) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, NSUB>;
   const uint64_t vd = st ? md.v1 : md.v0;
   const uint32_t p_base = tmem + C::TM_S + s * 128;
   const uint32_t d_tmem = tmem + C::TM_O + s * 128;
@@ -225,10 +231,10 @@ __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int 
 
 // Runs on one thread: the tensor pipe queues only a couple of MMAs, so any
 // cycle the issuing thread spends elsewhere between groups is idle tensor time.
-template <int D>
+template <int D, int NSUB>
 __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, NSUB>;
   MmaDescs md;
   md.q0 = smem_desc(smem_u32(smem + C::OFF_Q), 16, C::SBO, C::SWIZZLE);
   md.q1 = md.q0 + (uint64_t)(C::Q_BYTES >> 4);
@@ -245,7 +251,7 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
 #pragma unroll
   for (int sub = 0; sub < 2; ++sub) {
     if (u.n(sub) > 0) {
-      issue_s<D>(md, tmem, sub, 0, idesc_s);
+      issue_s<D, NSUB>(md, tmem, sub, 0, idesc_s);
       mma_commit(&sb.s_full[sub]);
     }
   }
@@ -260,12 +266,12 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
       if (i < u.n(sub)) {  // PV_sub(i)
         if (!mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.p_full[sub], i & 1, status)) return;
         tc_fence_after();
-        issue_pv<D>(md, tmem, sub, i & 1, i > 0, idesc_pv);
+        issue_pv<D, NSUB>(md, tmem, sub, i & 1, i > 0, idesc_pv);
         if (i == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
       }
       if (sub == 1) mma_commit(&sb.v_empty[i & 1]);  // every PV product of tile i is issued
       if (j < u.n(sub)) {  // S_sub(j)
-        issue_s<D>(md, tmem, sub, ks, idesc_s);
+        issue_s<D, NSUB>(md, tmem, sub, ks, idesc_s);
         mma_commit(&sb.s_full[sub]);
       }
     }
@@ -303,10 +309,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-template <int D, bool BF16>
+template <int D, int NSUB, bool BF16>
 __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, const FwdParams& p, const Unit u,
                                              int s) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, NSUB>;
   constexpr uint32_t FULL = 0xffffffffu;
   const int n = s ? u.n1 : u.n0;
   if (n == 0) return;
@@ -392,8 +398,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 #pragma unroll
       for (int k = 0; k < 4; ++k) pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
     }
-    const float rs0 = (ra0 + rb0) + (rc0 + rd0), rs1 = (ra1 + rb1) + (rc1 + rd1);
-    l_run = l_run * alpha + (rs0 + rs1);
+    l_run = l_run * alpha + (((ra0 + rb0) + (rc0 + rd0)) + ((ra1 + rb1) + (rc1 + rd1)));
 
     // Correction: O_s *= alpha for rows whose maximum moved.  PV_s(j-1) has
     // completed: the commit that signalled S_s(j) covers it.
@@ -444,15 +449,17 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 }
 
 // ----------------------------------------------------------------- kernel
-// Grid: x = 256-row query block counted from the last one, y = query head,
-// z = batch (or sequence).  CTAs are dispatched in that order, so the CTAs
-// running at any time mostly belong to a few heads and share their K/V tiles
-// in L2, and within a head the longest causal rows start first.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+// Grid: x = query block (NSUB * 128 rows) counted from the last one,
+// y = query head, z = batch (or sequence).  CTAs are dispatched in that order,
+// so the CTAs running at any time mostly belong to a few heads and share
+// their K/V tiles in L2, and within a head the longest causal rows start
+// first.  NSUB = 2 (two sub-tiles taking turns on the tensor core) is the
+// throughput configuration; NSUB = 1 gives small problems twice as many CTAs.
+template <int D, int NSUB, bool BF16>
+__global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, NSUB>;
   __shared__ SmemBarriers sb;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -481,7 +488,7 @@ __global__ void __launch_bounds__(384, 1)
   {
     const int first1 = u.row0 + C::BM;
     u.n0 = p.causal ? u.row0 / C::BN + 1 : n_all;  // row0 < L here
-    u.n1 = first1 >= u.L ? 0 : (p.causal ? first1 / C::BN + 1 : n_all);
+    u.n1 = (NSUB == 1 || first1 >= u.L) ? 0 : (p.causal ? first1 / C::BN + 1 : n_all);
   }
   u.n_max = max(u.n0, u.n1);
   const int warp = threadIdx.x >> 5;
@@ -501,16 +508,15 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&sb.p_full[i], 128);
       mbar_init(&sb.o_done[i], 1);
     }
-
     fence_mbar_init();
   }
-  if (warp == 8 && (threadIdx.x & 31) == 0) {
+  if (warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 9) {
-    tmem_alloc(&sb.tmem_base, 512);
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -518,28 +524,28 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = sb.tmem_base;
 
-  if (warp < 8) {
-    regs_grow<C::SOFTMAX_REGS>();
-    softmax_role<D, BF16>(sb, tmem, p, u, warp >> 2);
+  if (warp < 4 * NSUB) {
+    if constexpr (NSUB == 2) regs_grow<C::SOFTMAX_REGS>();
+    softmax_role<D, NSUB, BF16>(sb, tmem, p, u, warp >> 2);
   } else {
-    regs_shrink<C::CTRL_REGS>();
+    if constexpr (NSUB == 2) regs_shrink<C::CTRL_REGS>();
     const bool lane0 = (threadIdx.x & 31) == 0;
-    if (warp == 8) {
-      if (lane0) producer_role<D>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status);
+    if (warp == C::PRODUCER_WARP) {
+      if (lane0) producer_role<D, NSUB>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status);
       __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == C::MMA_WARP) {
       constexpr uint32_t ab = BF16 ? 1u : 0u;
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
-      if (lane0) mma_role<D>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+      if (lane0) mma_role<D, NSUB>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
       __syncwarp();
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 

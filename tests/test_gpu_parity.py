@@ -77,7 +77,7 @@ def test_small_workloads_full(name):
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w)
     o, lse = run_gpu(inp, w.causal)
-    compare_full(inp, o, lse, w.causal, w.scale, w.dtype)
+    compare_full(inp, o, lse, w.causal, w.scale, w.dtype, derived_ok=False)
 
 
 @pytest.mark.parametrize("name", ["c3", "c3_bnhd", "c4"])
@@ -100,3 +100,23 @@ def test_varlen_workload_sampled():
     rng = np.random.default_rng(1)
     pairs = [(s, (3 * s) % w.Hq) for s in range(len(w.seqlens))] + [(15, 0), (2, 15)]
     compare_sampled_varlen(inp, o.cpu(), lse.cpu(), w.causal, w.scale, w.dtype, pairs, rng)
+
+
+# The launch uses two 128-row sub-tiles per CTA when that still gives at least
+# one CTA per SM, and one sub-tile otherwise.  Many heads with short sequences
+# put ragged shapes on the two-sub-tile path (the small cases above take the
+# one-sub-tile path).
+@pytest.mark.parametrize("N", [129, 300, 511])
+@pytest.mark.parametrize("D,dt", [(64, "f16"), (128, "bf16"), (32, "bf16")])
+@pytest.mark.parametrize("causal", [True, False])
+def test_two_subtile_path_ragged(N, D, dt, causal):
+    inp = W.random_qkv(1, 152, 38, N, D, DT[dt], seed=N + 3 * D)
+    o, lse = run_gpu(inp, causal)
+    compare_full(inp, o, lse, causal, default_scale(D), DT[dt])
+
+
+def test_two_subtile_path_varlen():
+    lengths = [1, 200, 0, 257, 129, 700]
+    inp = W.random_varlen(lengths, 64, 16, 128, torch.bfloat16, seed=21)
+    o, lse = run_gpu(inp, True)
+    compare_full(inp, o, lse, True, default_scale(128), torch.bfloat16)
