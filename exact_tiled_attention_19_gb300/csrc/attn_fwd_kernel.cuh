@@ -346,8 +346,15 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     // Mask keys past the diagonal (causal) or past the sequence end.
     const int lim = last_key - j * C::BN;
     const bool masked = lim < C::BN - 1;
+    // Only diagonal and tail tiles need masking; the test is warp-uniform so
+    // that other tiles skip the per-element selects entirely.
+    const bool warp_masked = __any_sync(FULL, masked);
 #pragma unroll
-    for (int i = 0; i < C::BN / 2; ++i) sv[i] = (masked && i > lim) ? -INFINITY : __uint_as_float(sr[i]);
+    for (int i = 0; i < C::BN / 2; ++i) sv[i] = __uint_as_float(sr[i]);
+    if (warp_masked) {
+#pragma unroll
+      for (int i = 0; i < C::BN / 2; ++i) sv[i] = i > lim ? -INFINITY : sv[i];
+    }
     float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
     float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
 #pragma unroll
@@ -360,7 +367,11 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     tmem_ld_wait32(sr + 64);
     fence_regs32(sr + 96);
 #pragma unroll
-    for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = (masked && i > lim) ? -INFINITY : __uint_as_float(sr[i]);
+    for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = __uint_as_float(sr[i]);
+    if (warp_masked) {
+#pragma unroll
+      for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = i > lim ? -INFINITY : sv[i];
+    }
 #pragma unroll
     for (int i = C::BN / 2; i < C::BN; i += 8) {
       mx0 = max3(mx0, sv[i], sv[i + 1]);
