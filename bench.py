@@ -297,13 +297,13 @@ def blas_threads():
 def oracle_sample(w):
     """A bounded, deterministic slice of the workload for the CPU oracle:
     (description, list of (q_rows, k, v, positions) problems, convention FLOPs).
-    Packed batch: the sequence whose length is closest to 4096, every head.
+    Packed batch: the sequence whose length is closest to 10000, every head.
     Batched: batch 0, the first two query heads, every row."""
     from exact_tiled_attention_19_gb300 import workloads as W
     import torch
     g = torch.Generator().manual_seed(0)
     if w.layout == "varlen":
-        s = min(range(len(w.seqlens)), key=lambda i: abs(w.seqlens[i] - 4096))
+        s = min(range(len(w.seqlens)), key=lambda i: abs(w.seqlens[i] - 10000))
         L = w.seqlens[s]
         inp = W.make_inputs(w)
         t0 = int(inp["cu_seqlens"][s])
