@@ -322,7 +322,7 @@ def test_rows_api_matches_dense():
 
 def test_mutation_causal_mask_without_diagonal_is_caught(monkeypatch):
     monkeypatch.setattr(dense, "eligible_keys",
-                        lambda pos, L, causal: (np.arange(L)[None, :] < np.asarray(pos)[:, None]) if causal
+                        lambda pos, L, causal, *rest: (np.arange(L)[None, :] < np.asarray(pos)[:, None]) if causal
                         else np.ones((len(pos), L), dtype=bool))
     assert sdpa_error(1, 1, 1, 20, 8, True) > 1e-3
     assert not single_key_error() < 1e-3  # causal row 0 becomes empty (inf/nan error)
@@ -337,7 +337,7 @@ def test_mutation_wrong_gqa_mapping_is_caught(monkeypatch):
 def test_mutation_dropped_scale_is_caught(monkeypatch):
     orig = dense._rows_attention
     monkeypatch.setattr(dense, "_rows_attention",
-                        lambda q, pos, k, v, causal, scale: orig(q, pos, k, v, causal, 1.0))
+                        lambda q, pos, k, v, causal, scale, *rest: orig(q, pos, k, v, causal, 1.0, *rest))
     assert single_key_error() > 1e-3
     assert sdpa_error(1, 1, 1, 16, 16, True) > 1e-3
 
@@ -345,8 +345,8 @@ def test_mutation_dropped_scale_is_caught(monkeypatch):
 def test_mutation_lse_log2_is_caught(monkeypatch):
     orig = dense._rows_attention
 
-    def bad(q, pos, k, v, causal, scale):
-        o, lse = orig(q, pos, k, v, causal, scale)
+    def bad(q, pos, k, v, causal, scale, *rest):
+        o, lse = orig(q, pos, k, v, causal, scale, *rest)
         return o, lse / math.log(2.0)
     monkeypatch.setattr(dense, "_rows_attention", bad)
     assert lse_scipy_error(33, 8, True) > 1e-3
@@ -355,7 +355,7 @@ def test_mutation_lse_log2_is_caught(monkeypatch):
 def test_mutation_transposed_value_operand_is_caught(monkeypatch):
     orig = dense._rows_attention
     monkeypatch.setattr(dense, "_rows_attention",
-                        lambda q, pos, k, v, causal, scale: orig(q, pos, k, k, causal, scale))
+                        lambda q, pos, k, v, causal, scale, *rest: orig(q, pos, k, k, causal, scale, *rest))
     assert sdpa_error(1, 2, 2, 24, 8, False) > 1e-3
 
 
