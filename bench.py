@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; µs/call (1 GPU)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-PER_CONFIG = ["c1", "c2_causal", "c2_noncausal", "c2_large_logit", "c3", "c3_bnhd", "c4", "c5"]
+PER_CONFIG = ["c1", "c2_causal", "c2_noncausal", "c2_large_logit", "c3", "c3_bnhd", "c4", "c5",
+              "chunk2048_cache16384_gqa", "window4096_n16384"]
 
 
 def parse_args():
@@ -184,6 +185,8 @@ def device_inputs(w, device):
         T = sum(w.seqlens)
         dev["cu"] = inp["cu_seqlens"].to(device)
         dev["cu_host"] = inp["cu_seqlens"]
+        if "cu_seqlens_k" in inp:
+            dev["cu_k"] = inp["cu_seqlens_k"].to(device)
         dev["o"] = torch.empty((T, w.Hq, w.D), dtype=w.dtype, device=device)
         dev["lse"] = torch.empty((w.Hq, T), dtype=torch.float32, device=device)
     else:
@@ -194,14 +197,19 @@ def device_inputs(w, device):
 
 def make_call(w, dev, stream):
     from exact_tiled_attention_19_gb300 import binding
+    win = dict(window_left=w.window_left, window_right=w.window_right)
     if w.layout == "varlen":
+        kw = {}
+        if "cu_k" in dev:
+            kw = dict(cu_seqlens_k=dev["cu_k"], max_seqlen_k=max(w.seqlens_k))
+
         def call():
             binding.attention_varlen(dev["q"], dev["k"], dev["v"], dev["cu"], max(w.seqlens), causal=w.causal,
-                                     scale=w.scale, out=dev["o"], lse=dev["lse"], stream=stream)
+                                     scale=w.scale, out=dev["o"], lse=dev["lse"], stream=stream, **kw, **win)
     else:
         def call():
             binding.attention(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale, out=dev["o"],
-                              lse=dev["lse"], stream=stream)
+                              lse=dev["lse"], stream=stream, **win)
     return call
 
 
@@ -405,14 +413,16 @@ def correctness_gate(w, inp, dev):
             worst = max(worst, float(np.max(np.abs(f64(o[t0:t0 + L, 0][rows]) - ro))))
             worst = max(worst, float(np.max(np.abs(f64(lse[0, t0:t0 + L][rows]) - rl))))
     elif w.N * w.B * w.Hq <= 4096:
-        ro, rl = oracle.attention_dense(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), causal=w.causal, scale=w.scale)
+        ro, rl = oracle.attention_dense(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), causal=w.causal, scale=w.scale,
+                                        window_left=w.window_left, window_right=w.window_right)
         worst = max(float(np.max(np.abs(f64(o) - ro))), float(np.max(np.abs(f64(lse) - rl))))
     else:
         rows = np.array(sorted({0, 1, 127, 128, w.N // 2, w.N - 1}))
         for b, h in ((0, 0), (w.B - 1, w.Hq - 1)):
             hk = h // (w.Hq // w.Hkv)
             ro, rl = oracle.attention_rows(f64(inp["q"][b, h]), f64(inp["k"][b, hk]), f64(inp["v"][b, hk]), rows,
-                                           causal=w.causal, scale=w.scale)
+                                           causal=w.causal, scale=w.scale, window_left=w.window_left,
+                                           window_right=w.window_right)
             worst = max(worst, float(np.max(np.abs(f64(o[b, h][rows]) - ro))),
                         float(np.max(np.abs(f64(lse[b, h][rows]) - rl))))
     return worst <= tol, worst

@@ -1,11 +1,13 @@
 """ctypes binding of the C ABI in ``include/etattn.h``.
 
-The functions ``attn_fwd``, ``attn_fwd_varlen``, ``etattn_status_string``,
-``etattn_last_cuda_error``, ``etattn_read_device_status`` and
-``etattn_version`` have the C names and arguments (pointers as ints).  The
-helpers ``attention`` and ``attention_varlen`` marshal torch CUDA tensors
-(output allocation, strides, the current stream) and call them; every step of
-the computation runs in the library's kernels.  There is no fallback: if the
+The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_fwd_varlen``,
+``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
+``etattn_status_string``, ``etattn_last_cuda_error``,
+``etattn_read_device_status`` and ``etattn_version`` have the C names and
+arguments (pointers as ints).  The helpers ``attention`` and
+``attention_varlen`` marshal torch CUDA tensors (output allocation, strides,
+the current stream) and call them; every step of the computation runs in the
+library's kernels.  There is no fallback: if the
 library is missing or cannot be loaded, an error is raised.
 """
 
@@ -61,6 +63,10 @@ def load_library(path: str | None = None):
         lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _i64p, _int,
                                  ctypes.c_float, _vp]
         lib.attn_fwd.restype = _int
+        lib.attn_fwd_ex.argtypes = [_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _vp]
+        lib.attn_fwd_ex.restype = _int
+        lib.attn_fwd_varlen_ex.argtypes = [_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 3 + [ctypes.c_float, _vp]
+        lib.attn_fwd_varlen_ex.restype = _int
         lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                                         _int, _i64p, _int, ctypes.c_float, _vp]
         lib.attn_fwd_varlen.restype = _int
@@ -92,6 +98,26 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, dtype, strides, causal, scale, s
     lib = load_library()
     return lib.attn_fwd(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, N, D, dtype,
                         _strides_arg(strides), causal, scale, stream or None)
+
+
+def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                stream):
+    """C ``attn_fwd_ex``: pointers as ints (0 for NULL), ``strides`` 16 ints."""
+    lib = load_library()
+    return lib.attn_fwd_ex(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D, dtype,
+                           _strides_arg(strides), causal, window_left, window_right, scale, stream or None)
+
+
+def attn_fwd_varlen_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
+                       max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
+                       window_right, scale, stream):
+    """C ``attn_fwd_varlen_ex``: pointers (device offsets and optional host
+    mirrors) as ints; ``strides`` 12 ints."""
+    lib = load_library()
+    return lib.attn_fwd_varlen_ex(q or None, k or None, v or None, o or None, lse or None, cu_seqlens_q or None,
+                                  cu_seqlens_k or None, cu_seqlens_q_host or None, cu_seqlens_k_host or None,
+                                  num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype,
+                                  _strides_arg(strides), causal, window_left, window_right, scale, stream or None)
 
 
 def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, cu_seqlens_host, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D,
@@ -163,64 +189,98 @@ def _stream_handle(stream):
     return int(stream.cuda_stream)
 
 
-def attention(q, k, v, *, causal: bool = True, scale: float | None = None, out=None, lse=None,
-              return_lse: bool = True, stream=None):
+def attention(q, k, v, *, causal: bool = True, scale: float | None = None, window_left: int = -1,
+              window_right: int = -1, out=None, lse=None, return_lse: bool = True, stream=None):
     """Batched (GQA-capable) attention on CUDA tensors.
 
-    q: [B, Hq, N, D]; k, v: [B, Hkv, N, D] (any strides with d contiguous,
-    e.g. a [B, N, H, D] buffer viewed through permute).  Returns (o, lse) with
-    o a new [B, Hq, N, D] tensor (or ``out``) and lse a new [B, Hq, N] FP32
-    tensor (or ``lse``; None when ``return_lse`` is False)."""
+    q: [B, Hq, Nq, D]; k, v: [B, Hkv, Nk, D] (any strides with d contiguous,
+    e.g. a [B, N, H, D] buffer viewed through permute).  With Nk != Nq the
+    last query row aligns with the last key; ``window_left`` /
+    ``window_right`` >= 0 bound the keys a row reads around its own key
+    position.  Returns (o, lse) with o a new [B, Hq, Nq, D] tensor (or
+    ``out``) and lse a new [B, Hq, Nq] FP32 tensor (or ``lse``; None when
+    ``return_lse`` is False).  Square calls without a window go through
+    ``attn_fwd``, the others through ``attn_fwd_ex``."""
     import torch
-    B, Hq, N, D = q.shape
-    Hkv = k.shape[1]
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, Hq, N, D), dtype=q.dtype, device=q.device)
+        out = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
-        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, N) or not lse.is_contiguous()):
-        raise ValueError("lse must be a contiguous float32 [B, Hq, N] tensor")
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
     strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
+    lse_ptr = lse.data_ptr() if lse is not None else 0
+    square = Nq == Nk and window_left < 0 and window_right < 0
     with torch.cuda.device(q.device):
-        rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                      lse.data_ptr() if lse is not None else 0, B, Hq, Hkv, N, D, _dtype_code(q), strides,
-                      1 if causal else 0, float(scale), _stream_handle(stream))
+        if square:
+            rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, Nq, D,
+                          _dtype_code(q), strides, 1 if causal else 0, float(scale), _stream_handle(stream))
+        else:
+            rc = attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, Hq, Hkv, Nq, Nk,
+                             D, _dtype_code(q), strides, 1 if causal else 0, int(window_left), int(window_right),
+                             float(scale), _stream_handle(stream))
     if rc != 0:
-        raise EtattnError(rc, "attn_fwd")
+        raise EtattnError(rc, "attn_fwd" if square else "attn_fwd_ex")
     return out, lse
 
 
 def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = True, scale: float | None = None,
-                     cu_seqlens_host=None, out=None, lse=None, return_lse: bool = True, stream=None):
+                     cu_seqlens_k=None, max_seqlen_k: int | None = None, window_left: int = -1,
+                     window_right: int = -1, cu_seqlens_host=None, cu_seqlens_k_host=None, out=None, lse=None,
+                     return_lse: bool = True, stream=None):
     """Packed variable-length attention on CUDA tensors.
 
-    q: [T, Hq, D]; k, v: [T, Hkv, D]; cu_seqlens: int32 CUDA tensor [S+1].
-    ``cu_seqlens_host`` (optional int32 CPU tensor) is validated before launch.
-    Returns (o [T, Hq, D], lse [Hq, T] FP32 or None)."""
+    q: [T, Hq, D]; k, v: [Tk, Hkv, D]; cu_seqlens: int32 CUDA tensor [S+1]
+    of query offsets; ``cu_seqlens_k`` (default: cu_seqlens) the key
+    offsets, with ``max_seqlen_k`` their longest length.  The host mirrors
+    ``cu_seqlens_host`` / ``cu_seqlens_k_host`` (optional int32 CPU tensors)
+    are validated before launch.  Returns (o [T, Hq, D], lse [Hq, T] FP32 or
+    None).  Self-attention without a window goes through
+    ``attn_fwd_varlen``, the rest through ``attn_fwd_varlen_ex``."""
     import torch
     T, Hq, D = q.shape
-    Hkv = k.shape[1]
+    Tk, Hkv = k.shape[0], k.shape[1]
     S = cu_seqlens.shape[0] - 1
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
-        raise TypeError("cu_seqlens must be an int32 CUDA tensor")
+    for name, t in (("cu_seqlens", cu_seqlens), ("cu_seqlens_k", cu_seqlens_k)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_cuda):
+            raise TypeError(f"{name} must be an int32 CUDA tensor")
     if out is None:
         out = torch.empty((T, Hq, D), dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-    host_ptr = 0
-    if cu_seqlens_host is not None:
-        cu_seqlens_host = cu_seqlens_host.to(torch.int32).contiguous()
-        host_ptr = cu_seqlens_host.data_ptr()
+
+    def host_addr(t):
+        if t is None:
+            return None, 0
+        t = t.to(torch.int32).contiguous()
+        return t, t.data_ptr()
+
+    cu_host, host_ptr = host_addr(cu_seqlens_host)
+    cu_k_host, host_k_ptr = host_addr(cu_seqlens_k_host)
     strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
+    lse_ptr = lse.data_ptr() if lse is not None else 0
+    plain = cu_seqlens_k is None and cu_k_host is None and window_left < 0 and window_right < 0
     with torch.cuda.device(q.device):
-        rc = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             lse.data_ptr() if lse is not None else 0, cu_seqlens.data_ptr(), host_ptr, S,
-                             int(max_seqlen), T, Hq, Hkv, D, _dtype_code(q), strides, 1 if causal else 0,
-                             float(scale), _stream_handle(stream))
+        if plain:
+            rc = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                                 cu_seqlens.data_ptr(), host_ptr, S, int(max_seqlen), T, Hq, Hkv, D, _dtype_code(q),
+                                 strides, 1 if causal else 0, float(scale), _stream_handle(stream))
+        else:
+            cu_k = cu_seqlens if cu_seqlens_k is None else cu_seqlens_k
+            if cu_seqlens_k is None:
+                host_k_ptr = host_ptr
+            mk = int(max_seqlen if max_seqlen_k is None else max_seqlen_k)
+            rc = attn_fwd_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                                    cu_seqlens.data_ptr(), cu_k.data_ptr(), host_ptr, host_k_ptr, S, int(max_seqlen),
+                                    mk, T, Tk, Hq, Hkv, D, _dtype_code(q), strides, 1 if causal else 0,
+                                    int(window_left), int(window_right), float(scale), _stream_handle(stream))
+    del cu_host, cu_k_host
     if rc != 0:
-        raise EtattnError(rc, "attn_fwd_varlen")
+        raise EtattnError(rc, "attn_fwd_varlen" if plain else "attn_fwd_varlen_ex")
     return out, lse

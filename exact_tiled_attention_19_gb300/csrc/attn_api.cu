@@ -66,8 +66,11 @@ bool overlaps(const View& a, size_t ea, const View& b, size_t eb) {
   return alo < bhi && blo < ahi;
 }
 
-// d-stride 1; every other stride of an extent > 1 positive and a multiple of 16 bytes.
+// d-stride 1; every other stride of an extent > 1 positive and a multiple of
+// 16 bytes.  A view with an extent of 0 addresses nothing and passes.
 bool strides_ok(const View& v, size_t esz) {
+  for (int i = 0; i < v.rank; ++i)
+    if (v.size[i] == 0) return true;
   if (v.stride[v.rank - 1] != 1) return false;
   for (int i = 0; i < v.rank - 1; ++i) {
     if (v.size[i] <= 1) continue;
@@ -180,17 +183,23 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
 // Launch over `tokens` query rows per (head, batch/sequence).  Two 128-row
 // sub-tiles per CTA keep the tensor core busier, but halve the CTA count; a
 // problem that would not fill the GPU with two-sub-tile CTAs runs one
-// sub-tile per CTA instead.
+// sub-tile per CTA instead.  `general` selects the kernel built for unequal
+// query/key lengths and windows; square window-free calls take the other.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                   const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, cudaStream_t s) {
+                   const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, bool general,
+                   cudaStream_t s) {
   const bool bf = dtype == ETATTN_BF16;
   const int64_t blocks2 = (tokens + 255) / 256;
   const int nsub = blocks2 * (int64_t)gy * gz < num_sms ? 1 : 2;
   const dim3 g((unsigned)(nsub == 2 ? blocks2 : (tokens + 127) / 128), gy, gz);
   switch (D) {
-    case 32: return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, s) : launch_fwd_d32_0(q, k, v, p, g, nsub, s);
-    case 64: return bf ? launch_fwd_d64_1(q, k, v, p, g, nsub, s) : launch_fwd_d64_0(q, k, v, p, g, nsub, s);
-    default: return bf ? launch_fwd_d128_1(q, k, v, p, g, nsub, s) : launch_fwd_d128_0(q, k, v, p, g, nsub, s);
+    case 32:
+      return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, general, s) : launch_fwd_d32_0(q, k, v, p, g, nsub, general, s);
+    case 64:
+      return bf ? launch_fwd_d64_1(q, k, v, p, g, nsub, general, s) : launch_fwd_d64_0(q, k, v, p, g, nsub, general, s);
+    default:
+      return bf ? launch_fwd_d128_1(q, k, v, p, g, nsub, general, s)
+                : launch_fwd_d128_0(q, k, v, p, g, nsub, general, s);
   }
 }
 
@@ -203,27 +212,38 @@ using namespace etattn;
 
 namespace {
 
+// Effective key-window offsets: negative or huge means no bound; causal
+// attention caps the right offset at 0 (the diagonal).
+int window_left_of(int wl) { return (wl < 0 || wl > kUnboundedWindow) ? kUnboundedWindow : wl; }
+int window_right_of(int wr, int causal) {
+  if (causal) return 0;
+  return (wr < 0 || wr > kUnboundedWindow) ? kUnboundedWindow : wr;
+}
+
 // Validates every argument; launches only when do_launch is set.
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int D,
-             int dtype, const int64_t* strides, int causal, float scale, void* stream, bool do_launch) {
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+             int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
+             float scale, void* stream, bool do_launch) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
-  if (B < 0 || Hq < 0 || N < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
-  if (N > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
+  if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
+  if (Nq > kMaxTokens || Nk > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
-  if (B == 0 || Hq == 0 || N == 0) return ETATTN_OK;  // empty output: nothing to do
-  if (!q || !k || !v || !o) return ETATTN_ERR_NULL_PTR;
+  if (B == 0 || Hq == 0 || Nq == 0) return ETATTN_OK;  // empty output: nothing to do
+  const bool has_keys = Nk > 0;
+  if (!q || !o || (has_keys && (!k || !v))) return ETATTN_ERR_NULL_PTR;
 
-  const View vq{q, 4, {B, Hq, N, D}, {strides[0], strides[1], strides[2], strides[3]}};
-  const View vk{k, 4, {B, Hkv, N, D}, {strides[4], strides[5], strides[6], strides[7]}};
-  const View vv{v, 4, {B, Hkv, N, D}, {strides[8], strides[9], strides[10], strides[11]}};
-  const View vo{o, 4, {B, Hq, N, D}, {strides[12], strides[13], strides[14], strides[15]}};
-  const View vl{lse, 3, {B, Hq, N, 0}, {(int64_t)Hq * N, N, 1, 0}};
+  const View vq{q, 4, {B, Hq, Nq, D}, {strides[0], strides[1], strides[2], strides[3]}};
+  const View vk{k, 4, {B, Hkv, Nk, D}, {strides[4], strides[5], strides[6], strides[7]}};
+  const View vv{v, 4, {B, Hkv, Nk, D}, {strides[8], strides[9], strides[10], strides[11]}};
+  const View vo{o, 4, {B, Hq, Nq, D}, {strides[12], strides[13], strides[14], strides[15]}};
+  const View vl{lse, 3, {B, Hq, Nq, 0}, {(int64_t)Hq * Nq, Nq, 1, 0}};
   for (const View* t : {&vq, &vk, &vv, &vo})
     if (!strides_ok(*t, 2)) return ETATTN_ERR_BAD_STRIDE;
-  for (const void* ptr : {q, k, v, (const void*)o})
+  for (const void* ptr : {q, (const void*)o})
     if (!aligned16(ptr)) return ETATTN_ERR_BAD_ALIGN;
+  if (has_keys && (!aligned16(k) || !aligned16(v))) return ETATTN_ERR_BAD_ALIGN;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ETATTN_ERR_BAD_ALIGN;
   for (const View* t : {&vq, &vk, &vv})
     if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
@@ -237,9 +257,17 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
   CUtensorMap mq, mk, mv;
   bool swq = false, swk = false, swv = false;
-  if (int rc = encode_map(&mq, dtype, q, D, N, Hq, B, strides[2], strides[1], strides[0], &swq)) return rc;
-  if (int rc = encode_map(&mk, dtype, k, D, N, Hkv, B, strides[6], strides[5], strides[4], &swk)) return rc;
-  if (int rc = encode_map(&mv, dtype, v, D, N, Hkv, B, strides[10], strides[9], strides[8], &swv)) return rc;
+  if (int rc = encode_map(&mq, dtype, q, D, Nq, Hq, B, strides[2], strides[1], strides[0], &swq)) return rc;
+  if (has_keys) {
+    if (int rc = encode_map(&mk, dtype, k, D, Nk, Hkv, B, strides[6], strides[5], strides[4], &swk)) return rc;
+    if (int rc = encode_map(&mv, dtype, v, D, Nk, Hkv, B, strides[10], strides[9], strides[8], &swv)) return rc;
+  } else {
+    // No keys: every row is empty and the kernel loads no K/V tile; the
+    // query map stands in for the unused key and value maps.
+    mk = mq;
+    mv = mq;
+    swk = swv = swq;
+  }
 
   FwdParams p{};
   p.o = o;
@@ -247,56 +275,79 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.o_sb = strides[12];
   p.o_sh = strides[13];
   p.o_sn = strides[14];
-  p.lse_sb = (int64_t)Hq * N;
-  p.lse_sh = N;
-  p.cu_seqlens = nullptr;
-  p.N = N;
-  p.total_tokens = N;
-  p.max_seqlen = N;
+  p.lse_sb = (int64_t)Hq * Nq;
+  p.lse_sh = Nq;
+  p.cu_seqlens_q = p.cu_seqlens_k = nullptr;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.total_q = Nq;
+  p.total_k = Nk;
+  p.max_seqlen_q = Nq;
+  p.max_seqlen_k = Nk;
   p.Hq = Hq;
   p.group = Hq / Hkv;
-  p.causal = causal ? 1 : 0;
+  p.win_left = window_left_of(window_left);
+  p.win_right = window_right_of(window_right, causal);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, N, (unsigned)Hq, (unsigned)B, num_sms,
+  // Equal lengths and no left bound: every row reads key 0, so the square
+  // kernel applies whatever the right bound.
+  const bool general = Nq != Nk || p.win_left != kUnboundedWindow;
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, Nq, (unsigned)Hq, (unsigned)B, num_sms, general,
                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }
 
-int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
-                const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq, int Hkv,
-                int D, int dtype, const int64_t* strides, int causal, float scale, void* stream, bool do_launch) {
+// Host mirror of packed offsets: 0, non-decreasing, ending at total, every
+// length <= max_len.
+bool seqlens_ok(const int32_t* cu, int num_seqs, int total, int max_len) {
+  if (cu[0] != 0 || cu[num_seqs] != total) return false;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int64_t len = (int64_t)cu[s + 1] - cu[s];
+    if (len < 0 || len > max_len) return false;
+  }
+  return true;
+}
+
+int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_k_host,
+                int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int D,
+                int dtype, const int64_t* strides, int causal, int window_left, int window_right, float scale,
+                void* stream, bool do_launch) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
-  if (num_seqs < 0 || max_seqlen < 0 || total_tokens < 0 || Hq < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
-  if (max_seqlen > kMaxTokens || num_seqs > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
+  if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq < 0 ||
+      !head_dim_ok(D))
+    return ETATTN_ERR_BAD_SHAPE;
+  if (max_seqlen_q > kMaxTokens || max_seqlen_k > kMaxTokens || num_seqs > kMaxGridYZ || Hq > kMaxGridYZ)
+    return ETATTN_ERR_BAD_SHAPE;
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
-  if (cu_seqlens_host) {
-    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens) return ETATTN_ERR_BAD_SEQLENS;
-    for (int s = 0; s < num_seqs; ++s) {
-      const int64_t len = (int64_t)cu_seqlens_host[s + 1] - cu_seqlens_host[s];
-      if (len < 0 || len > max_seqlen) return ETATTN_ERR_BAD_SEQLENS;
-    }
-  }
-  if (num_seqs == 0 || Hq == 0 || total_tokens == 0 || max_seqlen == 0) return ETATTN_OK;
-  if (!q || !k || !v || !o || !cu_seqlens) return ETATTN_ERR_NULL_PTR;
+  if (cu_seqlens_q_host && !seqlens_ok(cu_seqlens_q_host, num_seqs, total_q, max_seqlen_q))
+    return ETATTN_ERR_BAD_SEQLENS;
+  if (cu_seqlens_k_host && !seqlens_ok(cu_seqlens_k_host, num_seqs, total_k, max_seqlen_k))
+    return ETATTN_ERR_BAD_SEQLENS;
+  if (num_seqs == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return ETATTN_OK;
+  const bool has_keys = total_k > 0;
+  if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || (has_keys && (!k || !v))) return ETATTN_ERR_NULL_PTR;
 
-  const int T = total_tokens;
+  const int T = total_q, Tk = total_k;
   const View vq{q, 3, {T, Hq, D, 0}, {strides[0], strides[1], strides[2], 0}};
-  const View vk{k, 3, {T, Hkv, D, 0}, {strides[3], strides[4], strides[5], 0}};
-  const View vv{v, 3, {T, Hkv, D, 0}, {strides[6], strides[7], strides[8], 0}};
+  const View vk{k, 3, {Tk, Hkv, D, 0}, {strides[3], strides[4], strides[5], 0}};
+  const View vv{v, 3, {Tk, Hkv, D, 0}, {strides[6], strides[7], strides[8], 0}};
   const View vo{o, 3, {T, Hq, D, 0}, {strides[9], strides[10], strides[11], 0}};
   const View vl{lse, 2, {Hq, T, 0, 0}, {T, 1, 0, 0}};
   for (const View* t : {&vq, &vk, &vv, &vo})
     if (!strides_ok(*t, 2)) return ETATTN_ERR_BAD_STRIDE;
-  for (const void* ptr : {q, k, v, (const void*)o})
+  for (const void* ptr : {q, (const void*)o})
     if (!aligned16(ptr)) return ETATTN_ERR_BAD_ALIGN;
+  if (has_keys && (!aligned16(k) || !aligned16(v))) return ETATTN_ERR_BAD_ALIGN;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ETATTN_ERR_BAD_ALIGN;
-  if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return ETATTN_ERR_BAD_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+    return ETATTN_ERR_BAD_ALIGN;
   for (const View* t : {&vq, &vk, &vv})
     if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
   if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
@@ -310,8 +361,14 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   CUtensorMap mq, mk, mv;
   bool swq = false, swk = false, swv = false;
   if (int rc = encode_map(&mq, dtype, q, D, T, Hq, 1, strides[0], strides[1], 0, &swq)) return rc;
-  if (int rc = encode_map(&mk, dtype, k, D, T, Hkv, 1, strides[3], strides[4], 0, &swk)) return rc;
-  if (int rc = encode_map(&mv, dtype, v, D, T, Hkv, 1, strides[6], strides[7], 0, &swv)) return rc;
+  if (has_keys) {
+    if (int rc = encode_map(&mk, dtype, k, D, Tk, Hkv, 1, strides[3], strides[4], 0, &swk)) return rc;
+    if (int rc = encode_map(&mv, dtype, v, D, Tk, Hkv, 1, strides[6], strides[7], 0, &swv)) return rc;
+  } else {
+    mk = mq;  // unused: no sequence has a key (see fwd_impl)
+    mv = mq;
+    swk = swv = swq;
+  }
 
   FwdParams p{};
   p.o = o;
@@ -321,18 +378,25 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.o_sn = strides[9];
   p.lse_sb = 0;
   p.lse_sh = T;
-  p.cu_seqlens = cu_seqlens;
-  p.N = 0;
-  p.total_tokens = T;
-  p.max_seqlen = max_seqlen;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.cu_seqlens_k = cu_seqlens_k;
+  p.Nq = p.Nk = 0;
+  p.total_q = T;
+  p.total_k = Tk;
+  p.max_seqlen_q = max_seqlen_q;
+  p.max_seqlen_k = max_seqlen_k;
   p.Hq = Hq;
   p.group = Hq / Hkv;
-  p.causal = causal ? 1 : 0;
+  p.win_left = window_left_of(window_left);
+  p.win_right = window_right_of(window_right, causal);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, max_seqlen, (unsigned)Hq, (unsigned)num_seqs, num_sms,
+  // Shared query and key offsets mean equal lengths in every sequence (see
+  // fwd_impl for why the right bound does not matter).
+  const bool general = cu_seqlens_k != cu_seqlens_q || p.win_left != kUnboundedWindow;
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, max_seqlen_q, (unsigned)Hq, (unsigned)num_seqs, num_sms, general,
                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
@@ -344,14 +408,32 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
              int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, D, dtype, strides, causal, scale, stream, true);
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, N, D, dtype, strides, causal, -1, -1, scale, stream, true);
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
+                float scale, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                  stream, true);
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
                     const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
                     int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream) {
-  return varlen_impl(q, k, v, o, lse, cu_seqlens, cu_seqlens_host, num_seqs, max_seqlen, total_tokens, Hq, Hkv, D,
-                     dtype, strides, causal, scale, stream, true);
+  return varlen_impl(q, k, v, o, lse, cu_seqlens, cu_seqlens, cu_seqlens_host, cu_seqlens_host, num_seqs, max_seqlen,
+                     max_seqlen, total_tokens, total_tokens, Hq, Hkv, D, dtype, strides, causal, -1, -1, scale, stream,
+                     true);
+}
+
+int attn_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
+                       const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                       int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides, int causal,
+                       int window_left, int window_right, float scale, void* stream) {
+  return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
+                     max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
+                     window_right, scale, stream, true);
 }
 
 int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
@@ -360,8 +442,8 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
   if ((lse_host == nullptr) != (lse_dev == nullptr)) return ETATTN_ERR_NULL_PTR;
   const int64_t st[16] = {(int64_t)Hq * N * D,  (int64_t)N * D, D, 1, (int64_t)Hkv * N * D, (int64_t)N * D, D, 1,
                           (int64_t)Hkv * N * D, (int64_t)N * D, D, 1, (int64_t)Hq * N * D,  (int64_t)N * D, D, 1};
-  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, D, dtype, st, causal, scale, stream,
-                        false))
+  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, N, D, dtype, st, causal, -1, -1, scale,
+                        stream, false))
     return rc;
   if (B == 0 || Hq == 0 || N == 0) return ETATTN_OK;
   if (!q_host || !k_host || !v_host || !o_host) return ETATTN_ERR_NULL_PTR;
@@ -371,8 +453,8 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
   if (e == cudaSuccess) e = cudaMemcpyAsync(k_dev, k_host, nkv, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(v_dev, v_host, nkv, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return fail_cuda(e);
-  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, D, dtype, st, causal, scale, stream,
-                        true))
+  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, N, D, dtype, st, causal, -1, -1, scale,
+                        stream, true))
     return rc;
   e = cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && lse_host)
@@ -388,8 +470,9 @@ int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_h
   if ((lse_host == nullptr) != (lse_dev == nullptr)) return ETATTN_ERR_NULL_PTR;
   if (cu_seqlens_host == nullptr) return ETATTN_ERR_NULL_PTR;
   const int64_t st[12] = {(int64_t)Hq * D, D, 1, (int64_t)Hkv * D, D, 1, (int64_t)Hkv * D, D, 1, (int64_t)Hq * D, D, 1};
-  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, cu_seqlens_host, num_seqs,
-                           max_seqlen, total_tokens, Hq, Hkv, D, dtype, st, causal, scale, stream, false))
+  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, cu_seqlens_dev, cu_seqlens_host,
+                           cu_seqlens_host, num_seqs, max_seqlen, max_seqlen, total_tokens, total_tokens, Hq, Hkv, D,
+                           dtype, st, causal, -1, -1, scale, stream, false))
     return rc;
   if (num_seqs == 0 || Hq == 0 || total_tokens == 0 || max_seqlen == 0) return ETATTN_OK;
   if (!q_host || !k_host || !v_host || !o_host) return ETATTN_ERR_NULL_PTR;
@@ -402,8 +485,9 @@ int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_h
   if (e == cudaSuccess) e = cudaMemcpyAsync(k_dev, k_host, nkv, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(v_dev, v_host, nkv, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return fail_cuda(e);
-  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, nullptr, num_seqs, max_seqlen,
-                           total_tokens, Hq, Hkv, D, dtype, st, causal, scale, stream, true))
+  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, cu_seqlens_dev, nullptr, nullptr,
+                           num_seqs, max_seqlen, max_seqlen, total_tokens, total_tokens, Hq, Hkv, D, dtype, st, causal,
+                           -1, -1, scale, stream, true))
     return rc;
   e = cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && lse_host)
@@ -423,7 +507,7 @@ const char* etattn_status_string(int code) {
     case ETATTN_ERR_BAD_ALIGN: return "a base pointer is not 16-byte aligned";
     case ETATTN_ERR_ALIAS: return "an output overlaps an input or the other output";
     case ETATTN_ERR_BAD_SCALE: return "scale must be finite and > 0";
-    case ETATTN_ERR_BAD_SEQLENS: return "bad cu_seqlens (must rise from 0 to total_tokens, lengths <= max_seqlen)";
+    case ETATTN_ERR_BAD_SEQLENS: return "bad cu_seqlens (must rise from 0 to the token total, lengths <= the max length)";
     case ETATTN_ERR_LAUNCH: return "a CUDA runtime call failed";
     case ETATTN_ERR_DEVICE: return "the device reported a failure (a bounded wait ran out)";
     case ETATTN_ERR_NO_DEVICE: return "no sm_103 CUDA device is current";
@@ -453,6 +537,6 @@ int etattn_read_device_status(int* out, int clear, void* stream) {
   return ETATTN_OK;
 }
 
-int etattn_version(void) { return 100; }
+int etattn_version(void) { return 200; }
 
 }  // extern "C"

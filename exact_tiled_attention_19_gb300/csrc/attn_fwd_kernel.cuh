@@ -11,6 +11,15 @@
 // mask keeps the diagonal; key tiles wholly in a row block's future are never
 // visited.  The epilogue writes O / l and lse = scale*m + ln l.
 //
+// Query and key lengths may differ ("Attention algorithms and data
+// movement", lesson 04): query row r of Lq sits at key position
+// c = r + Lk - Lq (the last query aligns with the last key).  Row r may read
+// keys lo <= j <= hi with hi = min(Lk - 1, c + win_right) and
+// lo = max(0, c - win_left); causal attention is win_right = 0, a local
+// window (same page, lesson 07) bounds win_left.  Each sub-tile streams only
+// the key tiles some of its rows may read, and a row that may read none gets
+// O = 0 and lse = -inf.
+//
 // A CTA owns 256 query rows as two sub-tiles (rows [0,128) and [128,256) of
 // the block).  Both read the same K/V tiles from shared memory.
 //
@@ -49,17 +58,24 @@
 
 namespace etattn {
 
+// Key-window bound meaning "no bound": any offset >= the longest sequence
+// acts the same, and c +/- kUnboundedWindow stays inside int32 for
+// |c| < 2^30.
+constexpr int kUnboundedWindow = (1 << 30) - 1;
+
 struct FwdParams {
   void* o;
   float* lse;
   int64_t o_sb, o_sh, o_sn;      // element strides of o (batch/sequence, head, token); d-stride 1
   int64_t lse_sb, lse_sh;        // element strides of lse (batch, head); token stride 1
-  const int* cu_seqlens;         // packed batch offsets, or nullptr for the batched layout
-  int N;                         // tokens per sequence (batched)
-  int total_tokens;              // packed batch: total tokens T
-  int max_seqlen;                // packed batch: bound on every length
+  const int* cu_seqlens_q;       // packed batch query offsets, or nullptr for the batched layout
+  const int* cu_seqlens_k;       // packed batch key offsets (may equal cu_seqlens_q)
+  int Nq, Nk;                    // batched: query / key tokens per sequence
+  int total_q, total_k;          // packed batch: total query / key tokens
+  int max_seqlen_q, max_seqlen_k;  // packed batch: bounds on every length
   int Hq, group;                 // query heads, Hq / Hkv
-  int causal;
+  int win_left, win_right;       // key j is eligible for a row at key position c iff
+                                 // c - win_left <= j <= c + win_right (causal: win_right = 0)
   float scale;                   // logit scale
   float scale_log2;              // scale * log2(e)
   int* status;                   // device status word
@@ -105,9 +121,9 @@ struct TileCfg {
   static constexpr int THREADS = NSUB == 2 ? 384 : 256;
   // Register split: 384 threads launch with LAUNCH_REGS each; warpgroup 2
   // (TMA + MMA) shrinks to CTRL_REGS so that the two softmax warpgroups can
-  // grow to SOFTMAX_REGS.  128*CTRL_REGS + 256*SOFTMAX_REGS == 384*LAUNCH_REGS.
+  // grow to SOFTMAX_REGS.  128*CTRL_REGS + 256*SOFTMAX_REGS <= 384*LAUNCH_REGS.
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = 88;
+  static constexpr int CTRL_REGS = 80;
   static constexpr int SOFTMAX_REGS = 208;
   static_assert(NSUB == 1 || 128 * CTRL_REGS + 256 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split over budget");
@@ -127,16 +143,33 @@ struct SmemBarriers {
   uint32_t tmem_base;
 };
 
-// Per-CTA work description shared by all roles.
+// Per-CTA work description shared by all roles.  Key tiles are streamed in
+// the order kt0, kt0 + 1, ..., kt0 + n_tot - 1; sub-tile s reads streamed
+// tiles f_s .. f_s + n_s - 1 of them (the two ranges overlap or touch).
 struct Unit {
   int h, hk, b, bcoord;          // query head, kv head, batch/sequence index, batch coordinate of the maps
-  int tok0;                      // first token of the sequence (packed batch), else 0
-  int L;                         // sequence length
+  int tok0q, tok0k;              // first query / key token of the sequence (packed batch), else 0
+  int Lq, Lk;                    // query / key length of the sequence
+  int delta;                     // Lk - Lq: query row r sits at key position r + delta
   int row0;                      // first query row (logical position) of sub-tile 0
-  int n0, n1;                    // key tiles visited by sub-tile 0 / 1 (0 = sub-tile idle)
+  int kt0, n_tot;                // first key tile streamed, tiles streamed
+  int f0, f1;                    // first streamed tile read by sub-tile 0 / 1
+  int n0, n1;                    // tiles read by sub-tile 0 / 1 (0 = nothing to read)
   __device__ __forceinline__ int n(int s) const { return s ? n1 : n0; }
-  int n_max;
+  __device__ __forceinline__ int f(int s) const { return s ? f1 : f0; }
+  // Sub-tile s reads streamed tile j.
+  __device__ __forceinline__ bool reads(int s, int j) const { return (unsigned)(j - f(s)) < (unsigned)n(s); }
 };
+
+// Key tiles [first, end) that some row of the query rows [r0, r0 + 128)
+// (clipped to the sequence) may read; {0, 0} when none may read any key.
+__device__ __forceinline__ int2 sub_tile_key_tiles(int r0, const Unit& u, const FwdParams& p, int bn) {
+  if (r0 >= u.Lq) return make_int2(0, 0);
+  const int c_first = r0 + u.delta, c_last = min(r0 + 127, u.Lq - 1) + u.delta;
+  const int lo = max(0, c_first - p.win_left), hi = min(u.Lk - 1, c_last + p.win_right);
+  if (hi < lo) return make_int2(0, 0);
+  return make_int2(lo / bn, hi / bn + 1);
+}
 
 // ----------------------------------------------------------------- producer
 // Runs on one thread.  (Waits are single-thread too: 32 lanes polling one
@@ -147,6 +180,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
                                               const Unit u, int hn_swapped, int* status) {
   using C = TileCfg<D, NSUB>;
   const bool swq = hn_swapped & 1, swk = (hn_swapped >> 1) & 1, swv = (hn_swapped >> 2) & 1;
+  if (u.n_tot == 0) return;  // no row of this CTA reads a key
   {
     mbar_arrive_expect_tx(&sb.q_full, NSUB * C::Q_BYTES);
 #pragma unroll
@@ -154,10 +188,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_Q + s * C::Q_BYTES + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full,
-                      c * C::SW_ELEMS, u.tok0 + u.row0 + s * C::BM, u.h, u.bcoord, swq);
+                      c * C::SW_ELEMS, u.tok0q + u.row0 + s * C::BM, u.h, u.bcoord, swq);
   }
   int ks = 0, kph = 0;  // K ring slot and its phase for tile j
-  for (int j = 0; j < u.n_max; ++j) {
+  for (int j = 0; j < u.n_tot; ++j) {
+    const int key0 = u.tok0k + (u.kt0 + j) * C::BN;
     // K_j goes to slot j % 3, whose previous tile j-3 must have been released.
     if (j >= C::K_STAGES && !mbar_wait(&sb.k_empty[ks], kph ^ 1, status)) return;
     {
@@ -165,7 +200,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_K + ks * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmK, &sb.k_full[ks],
-                      c * C::SW_ELEMS, u.tok0 + j * C::BN, u.hk, u.bcoord, swk);
+                      c * C::SW_ELEMS, key0, u.hk, u.bcoord, swk);
     }
     if (++ks == C::K_STAGES) {
       ks = 0;
@@ -178,7 +213,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_V + vs * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmV, &sb.v_full[vs],
-                      c * C::SW_ELEMS, u.tok0 + j * C::BN, u.hk, u.bcoord, swv);
+                      c * C::SW_ELEMS, key0, u.hk, u.bcoord, swv);
     }
   }
 }
@@ -231,7 +266,9 @@ __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int 
 
 // Runs on one thread: the tensor pipe queues only a couple of MMAs, so any
 // cycle the issuing thread spends elsewhere between groups is idle tensor time.
-template <int D, int NSUB>
+// GEN = false is the square, window-free case, where both sub-tiles start at
+// streamed tile 0 and the per-tile range tests fold away at compile time.
+template <int D, int NSUB, bool GEN>
 __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
   using C = TileCfg<D, NSUB>;
@@ -243,6 +280,10 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
   md.k2 = md.k1 + (uint64_t)(C::KV_BYTES >> 4);
   md.v0 = smem_desc(smem_u32(smem + C::OFF_V), C::BN * C::SW_BYTES, C::SBO, C::SWIZZLE);
   md.v1 = md.v0 + (uint64_t)(C::KV_BYTES >> 4);
+  // Sub-tile `sub` reads streamed tile j; its own count of that tile.
+  auto reads = [&](int sub, int j) { return GEN ? u.reads(sub, j) : j < u.n(sub); };
+  auto own = [&](int sub, int j) { return GEN ? j - u.f(sub) : j; };
+  if (u.n_tot == 0) return;  // no row of this CTA reads a key
   if (!mbar_wait(&sb.q_full, 0, status)) return;
 
   int ks = 0, kph = 0;  // K ring slot / phase of the next key tile
@@ -250,27 +291,31 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
   tc_fence_after();
 #pragma unroll
   for (int sub = 0; sub < 2; ++sub) {
-    if (u.n(sub) > 0) {
+    if (reads(sub, 0)) {
       issue_s<D, NSUB>(md, tmem, sub, 0, idesc_s);
       mma_commit(&sb.s_full[sub]);
     }
   }
   mma_commit(&sb.k_empty[0]);
   ks = 1;
-  for (int j = 1; j <= u.n_max; ++j) {
+  // Step j issues the PV products of streamed tile j - 1 and the S products
+  // of tile j, interleaved by sub-tile.
+  for (int j = 1; j <= u.n_tot; ++j) {
     const int i = j - 1;  // key tile whose PV products are issued in this step
-    const bool has_k = j < u.n_max;
+    const bool has_k = j < u.n_tot;
     if (has_k && !mbar_wait(&sb.k_full[ks], kph, status)) return;
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
-      if (i < u.n(sub)) {  // PV_sub(i)
-        if (!mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.p_full[sub], i & 1, status)) return;
+      if (reads(sub, i)) {  // PV_sub(i)
+        const int li = own(sub, i);
+        if (!mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.p_full[sub], li & 1, status))
+          return;
         tc_fence_after();
-        issue_pv<D, NSUB>(md, tmem, sub, i & 1, i > 0, idesc_pv);
-        if (i == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
+        issue_pv<D, NSUB>(md, tmem, sub, i & 1, li > 0, idesc_pv);
+        if (li == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
       }
       if (sub == 1) mma_commit(&sb.v_empty[i & 1]);  // every PV product of tile i is issued
-      if (j < u.n(sub)) {  // S_sub(j)
+      if (has_k && reads(sub, j)) {  // S_sub(j)
         issue_s<D, NSUB>(md, tmem, sub, ks, idesc_s);
         mma_commit(&sb.s_full[sub]);
       }
@@ -286,9 +331,9 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
   // Drain: wait for the commit arrivals nobody else consumes (the last
   // tiles' ring releases and the final PV of each sub-tile) so that no
   // arrival can land in shared memory after the CTA exits.
-  for (int t = u.n_max > C::K_STAGES ? u.n_max - C::K_STAGES : 0; t < u.n_max; ++t)
+  for (int t = u.n_tot > C::K_STAGES ? u.n_tot - C::K_STAGES : 0; t < u.n_tot; ++t)
     if (!mbar_wait(&sb.k_empty[t % C::K_STAGES], (t / C::K_STAGES) & 1, status)) return;
-  for (int t = u.n_max >= 2 ? u.n_max - 2 : 0; t < u.n_max; ++t)
+  for (int t = u.n_tot >= 2 ? u.n_tot - 2 : 0; t < u.n_tot; ++t)
     if (!mbar_wait(&sb.v_empty[t & 1], (t >> 1) & 1, status)) return;
 #pragma unroll
   for (int sub = 0; sub < 2; ++sub)
@@ -309,23 +354,44 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-template <int D, int NSUB, bool BF16>
+// GEN = false is the square, window-free case: every row reads key 0 in the
+// first tile, so no row meets a tile with m = -inf and no lower edge exists.
+template <int D, int NSUB, bool BF16, bool GEN>
 __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, const FwdParams& p, const Unit u,
                                              int s) {
   using C = TileCfg<D, NSUB>;
   constexpr uint32_t FULL = 0xffffffffu;
-  const int n = s ? u.n1 : u.n0;
-  if (n == 0) return;
+  const int n = u.n(s);
   const int t = threadIdx.x & 127;  // query row inside the sub-tile = tensor-memory lane
+  const int row_pos = u.row0 + s * C::BM + t;  // logical position inside the query sequence
+  const bool valid = row_pos < u.Lq;
+  // Output row and lse addresses (formed where they are used, so that they
+  // hold no registers across the tile loop).
+  auto o_row = [&]() {
+    return reinterpret_cast<uint8_t*>(p.o) +
+           2 * ((int64_t)u.b * p.o_sb + (int64_t)u.h * p.o_sh + (int64_t)(u.tok0q + row_pos) * p.o_sn);
+  };
+  auto lse_at = [&]() { return p.lse + ((int64_t)u.b * p.lse_sb + (int64_t)u.h * p.lse_sh + u.tok0q + row_pos); };
+  if (n == 0) {  // no row of this sub-tile may read a key: O = 0, lse = -inf
+    if (valid) {
+      uint8_t* orow = o_row();
+#pragma unroll
+      for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c * 2) = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse != nullptr) *lse_at() = -INFINITY;
+    }
+    return;
+  }
   const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
   const uint32_t tS = tmem + C::TM_S + s * 128 + lane_off;
   const uint32_t tO = tmem + C::TM_O + s * 128 + lane_off;
-  const int row_pos = u.row0 + s * C::BM + t;  // logical position inside the sequence
   const float c2 = p.scale_log2;
   int* status = p.status;
-  // Last eligible key position of this row: the diagonal under the causal
-  // mask, and never past the end of the sequence.
-  const int last_key = p.causal ? min(row_pos, u.L - 1) : u.L - 1;
+  // Keys this row may read, as offsets from the first key of the current
+  // tile: lim_lo <= i <= lim_hi.  Both move down by one tile per step.
+  const int c_row = row_pos + u.delta;
+  const int kb0 = (u.kt0 + u.f(s)) * C::BN;
+  int lim_hi = min(u.Lk - 1, c_row + p.win_right) - kb0;
+  int lim_lo = max(0, c_row - p.win_left) - kb0;
   float m_run = -INFINITY;  // running maximum of the raw scores (scale > 0)
   float l_run = 0.f;        // sum of exp2(c2 * (s - m_run)) over the keys seen
 
@@ -343,17 +409,20 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     tmem_ld_x32(tS + 96, sr + 96);
 
     float sv[C::BN];
-    // Mask keys past the diagonal (causal) or past the sequence end.
-    const int lim = last_key - j * C::BN;
-    const bool masked = lim < C::BN - 1;
-    // Only diagonal and tail tiles need masking; the test is warp-uniform so
-    // that other tiles skip the per-element selects entirely.
-    const bool warp_masked = __any_sync(FULL, masked);
+    // Mask keys past the diagonal (causal), the window or the sequence end.
+    // Only tiles on those edges need masking; the tests are warp-uniform so
+    // that other tiles skip the per-element selects entirely, and a lower
+    // edge (a window's left end) exists only for windowed calls.
+    const bool warp_masked = __any_sync(FULL, GEN ? (lim_hi < C::BN - 1 || lim_lo > 0) : lim_hi < C::BN - 1);
+    const bool warp_lower = GEN && warp_masked && __any_sync(FULL, lim_lo > 0);
 #pragma unroll
     for (int i = 0; i < C::BN / 2; ++i) sv[i] = __uint_as_float(sr[i]);
-    if (warp_masked) {
+    if (warp_lower) {
 #pragma unroll
-      for (int i = 0; i < C::BN / 2; ++i) sv[i] = i > lim ? -INFINITY : sv[i];
+      for (int i = 0; i < C::BN / 2; ++i) sv[i] = (i > lim_hi || i < lim_lo) ? -INFINITY : sv[i];
+    } else if (warp_masked) {
+#pragma unroll
+      for (int i = 0; i < C::BN / 2; ++i) sv[i] = i > lim_hi ? -INFINITY : sv[i];
     }
     float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
     float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
@@ -368,10 +437,15 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     fence_regs32(sr + 96);
 #pragma unroll
     for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = __uint_as_float(sr[i]);
-    if (warp_masked) {
+    if (warp_lower) {
 #pragma unroll
-      for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = i > lim ? -INFINITY : sv[i];
+      for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = (i > lim_hi || i < lim_lo) ? -INFINITY : sv[i];
+    } else if (warp_masked) {
+#pragma unroll
+      for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = i > lim_hi ? -INFINITY : sv[i];
     }
+    lim_hi -= C::BN;
+    lim_lo -= C::BN;
 #pragma unroll
     for (int i = C::BN / 2; i < C::BN; i += 8) {
       mx0 = max3(mx0, sv[i], sv[i + 1]);
@@ -382,14 +456,17 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
     const float m_new = fmaxf(m_run, m_tile);
     // Lazy rescale: move the reference maximum only when it grows by more
-    // than 8 in log2 units (always on the first tile).
+    // than 8 in log2 units (always on the first tile, and always when the row
+    // sees its first eligible key: -inf to finite compares as +inf > 8).
     const bool rescale = (j == 0) || (m_new - m_run) * c2 > 8.f;
     float alpha = 1.f;
     if (rescale) {
       alpha = (j == 0) ? 0.f : ex2_approx((m_run - m_new) * c2);
       m_run = m_new;
     }
-    const float neg_mc = -m_run * c2;
+    // A row that has not met an eligible key yet keeps m = -inf; its masked
+    // scores must still give p = exp2(-inf) = 0, not exp2(-inf + inf).
+    const float neg_mc = (GEN && m_run == -INFINITY) ? 0.f : -m_run * c2;
     // p = exp2(s * c2 - m * c2): the scaling runs two lanes per instruction,
     // the row sum in four independent pairs of accumulators.
     uint32_t pk[C::BN / 2];
@@ -431,13 +508,14 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     mbar_arrive(&sb.p_full[s]);
   }
 
-  // Epilogue: O = O_acc / l in the input type, lse = scale * m + ln l.
+  // Epilogue: O = O_acc / l in the input type, lse = scale * m + ln l.  A
+  // row that met no eligible key has l = 0 and O_acc = 0 (every p was 0):
+  // it gets O = 0 and lse = -inf.
   if (!warp_wait(&sb.o_done[s], 0, status)) return;
   tc_fence_after();
-  const bool valid = row_pos < u.L;
-  const float inv_l = 1.f / l_run;
-  uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                  2 * ((int64_t)u.b * p.o_sb + (int64_t)u.h * p.o_sh + (int64_t)(u.tok0 + row_pos) * p.o_sn);
+  const bool nonempty = l_run > 0.f;
+  const float inv_l = nonempty ? 1.f / l_run : 0.f;
+  uint8_t* orow = o_row();
 #pragma unroll
   for (int c = 0; c < D; c += 32) {
     uint32_t o[32];
@@ -455,8 +533,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
       dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
     }
   }
-  if (valid && p.lse != nullptr)
-    p.lse[(int64_t)u.b * p.lse_sb + (int64_t)u.h * p.lse_sh + u.tok0 + row_pos] = m_run * p.scale + __logf(l_run);
+  if (valid && p.lse != nullptr) *lse_at() = nonempty ? m_run * p.scale + __logf(l_run) : -INFINITY;
 }
 
 // ----------------------------------------------------------------- kernel
@@ -466,7 +543,9 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 // their K/V tiles in L2, and within a head the longest causal rows start
 // first.  NSUB = 2 (two sub-tiles taking turns on the tensor core) is the
 // throughput configuration; NSUB = 1 gives small problems twice as many CTAs.
-template <int D, int NSUB, bool BF16>
+// GEN = true handles unequal lengths and windows; the square, window-free
+// case compiles without their per-tile tests (they cost about 3% there).
+template <int D, int NSUB, bool BF16, bool GEN>
 __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -479,29 +558,39 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   u.h = blockIdx.y;
   u.b = blockIdx.z;
   u.hk = u.h / p.group;
-  u.L = p.N;
-  u.tok0 = 0;
+  u.Lq = p.Nq;
+  u.Lk = p.Nk;
+  u.tok0q = u.tok0k = 0;
   u.bcoord = u.b;
-  if (p.cu_seqlens != nullptr) {
-    const int s0 = p.cu_seqlens[u.b], s1 = p.cu_seqlens[u.b + 1];
-    if (s0 < 0 || s1 < s0 || s1 > p.total_tokens || s1 - s0 > p.max_seqlen) {
+  if (p.cu_seqlens_q != nullptr) {
+    const int q0 = p.cu_seqlens_q[u.b], q1 = p.cu_seqlens_q[u.b + 1];
+    const int k0 = p.cu_seqlens_k[u.b], k1 = p.cu_seqlens_k[u.b + 1];
+    if (q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.max_seqlen_q || k0 < 0 || k1 < k0 ||
+        k1 > p.total_k || k1 - k0 > p.max_seqlen_k) {
       if (threadIdx.x == 0) atomicCAS(p.status, 0, (int)kDevBadSeqlens);
       return;
     }
-    u.L = s1 - s0;
-    u.tok0 = s0;
+    u.Lq = q1 - q0;
+    u.Lk = k1 - k0;
+    u.tok0q = q0;
+    u.tok0k = k0;
     u.bcoord = 0;
   }
   const int block = (int)gridDim.x - 1 - (int)blockIdx.x;
   u.row0 = block * C::BLOCK_M;
-  if (u.row0 >= u.L) return;  // uniform across the CTA
-  const int n_all = (u.L + C::BN - 1) / C::BN;
+  if (u.row0 >= u.Lq) return;  // uniform across the CTA
+  u.delta = u.Lk - u.Lq;
   {
-    const int first1 = u.row0 + C::BM;
-    u.n0 = p.causal ? u.row0 / C::BN + 1 : n_all;  // row0 < L here
-    u.n1 = (NSUB == 1 || first1 >= u.L) ? 0 : (p.causal ? first1 / C::BN + 1 : n_all);
+    const int2 r0 = sub_tile_key_tiles(u.row0, u, p, C::BN);
+    const int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + C::BM, u, p, C::BN) : make_int2(0, 0);
+    const bool a0 = r0.y > r0.x, a1 = r1.y > r1.x;
+    u.kt0 = a0 ? (a1 ? min(r0.x, r1.x) : r0.x) : (a1 ? r1.x : 0);
+    u.n_tot = (a0 || a1) ? max(a0 ? r0.y : 0, a1 ? r1.y : 0) - u.kt0 : 0;
+    u.f0 = a0 ? r0.x - u.kt0 : 0;
+    u.n0 = a0 ? r0.y - r0.x : 0;
+    u.f1 = a1 ? r1.x - u.kt0 : 0;
+    u.n1 = a1 ? r1.y - r1.x : 0;
   }
-  u.n_max = max(u.n0, u.n1);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -537,7 +626,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
 
   if (warp < 4 * NSUB) {
     if constexpr (NSUB == 2) regs_grow<C::SOFTMAX_REGS>();
-    softmax_role<D, NSUB, BF16>(sb, tmem, p, u, warp >> 2);
+    softmax_role<D, NSUB, BF16, GEN>(sb, tmem, p, u, warp >> 2);
   } else {
     if constexpr (NSUB == 2) regs_shrink<C::CTRL_REGS>();
     const bool lane0 = (threadIdx.x & 31) == 0;
@@ -548,7 +637,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
       constexpr uint32_t ab = BF16 ? 1u : 0u;
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
-      if (lane0) mma_role<D, NSUB>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+      if (lane0) mma_role<D, NSUB, GEN>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
       __syncwarp();
     }
   }

@@ -16,6 +16,9 @@ Recipe (the pages fix no data; these readings are stated once here):
     are concatenated in sequence order and located by ``cu_seqlens``.
   * The transposed layout stores the same logical [B, H, N, D] values
     contiguously as [B, N, H, D] and is addressed through strides.
+  * Workloads with Nk != Nq (a chunk of new queries over a longer key
+    cache) draw K and V with Nk tokens; packed batches with separate key
+    lengths draw Tk = sum of key lengths.  The draw order stays q, k, v.
 """
 
 from __future__ import annotations
@@ -23,6 +26,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass, field
 
+import numpy as np
 import torch
 
 # Lengths drawn by torch.randint(1, 16385, (16,), generator=Generator().manual_seed(7)).
@@ -44,34 +48,78 @@ class Workload:
     layout: str = "bhnd"          # "bhnd" | "bnhd" | "varlen"
     q_scale: float = 1.0          # multiplier on the float32 Q draw
     seqlens: tuple = field(default_factory=tuple)
+    Nk: int | None = None         # key tokens per sequence (batched); None = N
+    seqlens_k: tuple = field(default_factory=tuple)  # packed key lengths; empty = seqlens
+    window_left: int = -1         # local window (keys before the row's key position); -1 = none
+    window_right: int = -1
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.D)
 
     @property
+    def keys(self) -> int:
+        return self.N if self.Nk is None else self.Nk
+
+    def lengths(self):
+        """(query length, key length) of every sequence."""
+        if self.layout == "varlen":
+            lk = self.seqlens_k or self.seqlens
+            return list(zip(self.seqlens, lk))
+        return [(self.N, self.keys)] * self.B
+
+    @property
     def total_tokens(self) -> int:
-        return sum(self.seqlens) if self.layout == "varlen" else self.B * self.N
+        return sum(lq for lq, _ in self.lengths())
+
+    @property
+    def total_keys(self) -> int:
+        return sum(lk for _, lk in self.lengths())
+
+    @property
+    def square(self) -> bool:
+        """Equal query and key lengths and no window."""
+        return all(lq == lk for lq, lk in self.lengths()) and self.window_left < 0 and self.window_right < 0
 
     def flops_convention(self) -> float:
-        """4 * N^2 * D per (sequence, query head), halved when causal."""
-        lens = self.seqlens if self.layout == "varlen" else [self.N] * self.B
-        f = sum(4.0 * L * L * self.D for L in lens) * self.Hq
+        """4 * N^2 * D per (sequence, query head), halved when causal.  For
+        unequal lengths or a window, the exact count."""
+        if not self.square:
+            return self.flops_exact()
+        f = sum(4.0 * lq * lk * self.D for lq, lk in self.lengths()) * self.Hq
         return f / 2 if self.causal else f
 
+    def eligible_pairs(self) -> int:
+        """(query row, key) pairs that enter the softmax, per query head,
+        summed over sequences.  Query row r of Lq sits at key position
+        r + Lk - Lq; the causal mask and a window bound the keys it reads."""
+        total = 0
+        for lq, lk in self.lengths():
+            if lq == 0 or lk == 0:
+                continue
+            c = np.arange(lq, dtype=np.int64) + (lk - lq)
+            hi = np.full(lq, lk - 1, dtype=np.int64)
+            if self.causal:
+                hi = np.minimum(hi, c)
+            if self.window_right >= 0:
+                hi = np.minimum(hi, c + self.window_right)
+            lo = np.zeros(lq, dtype=np.int64)
+            if self.window_left >= 0:
+                lo = np.maximum(lo, c - self.window_left)
+            total += int(np.maximum(hi - lo + 1, 0).sum())
+        return total
+
     def flops_exact(self) -> float:
-        """Multiply-adds actually required: causal rows see i+1 keys."""
-        lens = self.seqlens if self.layout == "varlen" else [self.N] * self.B
-        if self.causal:
-            return sum(4.0 * self.D * L * (L + 1) / 2 for L in lens) * self.Hq
-        return self.flops_convention()
+        """Multiply-adds actually required: 4 * D per eligible pair (QK^T and
+        PV, two flops per multiply-add each)."""
+        return 4.0 * self.D * self.eligible_pairs() * self.Hq
 
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes of one call: read Q, K, V once, write O and
         the FP32 logsumexp once."""
         esz = torch.tensor([], dtype=self.dtype).element_size()
-        tq = self.total_tokens
-        return (2 * tq * self.Hq * self.D + 2 * tq * self.Hkv * self.D) * esz + tq * self.Hq * 4
+        tq, tk = self.total_tokens, self.total_keys
+        return (2 * tq * self.Hq * self.D + 2 * tk * self.Hkv * self.D) * esz + tq * self.Hq * 4
 
 
 WORKLOADS = {
@@ -91,6 +139,13 @@ WORKLOADS = {
     "c5": Workload("c5", "packed varlen, 16 sequences (seed 7), H=16, D=128, BF16, causal", 1, 16, 16,
                    max(VARLEN_LENGTHS_SEED7), 128, torch.bfloat16, True, layout="varlen",
                    seqlens=tuple(VARLEN_LENGTHS_SEED7)),
+    # Unequal lengths and local windows.
+    "chunk2048_cache16384_gqa": Workload(
+        "chunk2048_cache16384_gqa", "GQA B=2, Hq=32, Hkv=8, 2048 new queries over 16384 keys (bottom-right causal), "
+        "D=128, BF16", 2, 32, 8, 2048, 128, torch.bfloat16, True, Nk=16384),
+    "window4096_n16384": Workload(
+        "window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys (diagonal included), D=128, BF16",
+        2, 16, 16, 16384, 128, torch.bfloat16, True, window_left=4095),
 }
 
 
@@ -124,26 +179,30 @@ def make_inputs(w: Workload | str, seed: int = 0):
         w = WORKLOADS[w]
     g = torch.Generator().manual_seed(seed)
     if w.layout == "varlen":
-        T = sum(w.seqlens)
+        T, Tk = w.total_tokens, w.total_keys
         q = _draw((T, w.Hq, w.D), g, w.dtype, w.q_scale)
-        k = _draw((T, w.Hkv, w.D), g, w.dtype)
-        v = _draw((T, w.Hkv, w.D), g, w.dtype)
-        return {"q": q, "k": k, "v": v, "cu_seqlens": cu_seqlens_of(w.seqlens)}
+        k = _draw((Tk, w.Hkv, w.D), g, w.dtype)
+        v = _draw((Tk, w.Hkv, w.D), g, w.dtype)
+        out = {"q": q, "k": k, "v": v, "cu_seqlens": cu_seqlens_of(w.seqlens)}
+        if w.seqlens_k:
+            out["cu_seqlens_k"] = cu_seqlens_of(w.seqlens_k)
+        return out
     q = _draw((w.B, w.Hq, w.N, w.D), g, w.dtype, w.q_scale)
-    k = _draw((w.B, w.Hkv, w.N, w.D), g, w.dtype)
-    v = _draw((w.B, w.Hkv, w.N, w.D), g, w.dtype)
+    k = _draw((w.B, w.Hkv, w.keys, w.D), g, w.dtype)
+    v = _draw((w.B, w.Hkv, w.keys, w.D), g, w.dtype)
     if w.layout == "bnhd":
         q, k, v = (t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3) for t in (q, k, v))
     return {"q": q, "k": k, "v": v}
 
 
-def random_qkv(B, Hq, Hkv, N, D, dtype, seed=0, layout="bhnd", q_scale=1.0):
+def random_qkv(B, Hq, Hkv, N, D, dtype, seed=0, layout="bhnd", q_scale=1.0, Nk=None):
     """Small seeded inputs of arbitrary shape (same recipe as make_inputs)."""
-    w = Workload("adhoc", "adhoc", B, Hq, Hkv, N, D, dtype, True, layout=layout, q_scale=q_scale)
+    w = Workload("adhoc", "adhoc", B, Hq, Hkv, N, D, dtype, True, layout=layout, q_scale=q_scale, Nk=Nk)
     return make_inputs(w, seed)
 
 
-def random_varlen(lengths, Hq, Hkv, D, dtype, seed=0, q_scale=1.0):
+def random_varlen(lengths, Hq, Hkv, D, dtype, seed=0, q_scale=1.0, lengths_k=None):
     w = Workload("adhoc_varlen", "adhoc", 1, Hq, Hkv, max(lengths) if lengths else 0, D, dtype, True,
-                 layout="varlen", q_scale=q_scale, seqlens=tuple(int(x) for x in lengths))
+                 layout="varlen", q_scale=q_scale, seqlens=tuple(int(x) for x in lengths),
+                 seqlens_k=tuple(int(x) for x in lengths_k) if lengths_k is not None else ())
     return make_inputs(w, seed)

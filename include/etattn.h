@@ -13,11 +13,22 @@
  * rescaling both the numerator accumulator and the denominator whenever the
  * maximum grows, without ever materialising the score matrix.  E(i) is every
  * key, or under the causal mask the keys j <= i (the diagonal is included, so
- * no causal row is empty).  Grouped-query attention ("Attention algorithms and
- * data movement", lesson 05): query head h reads key/value head
- * h / (Hq / Hkv).  Packed variable-length batches (same page, lesson 04):
- * positions are logical positions inside each sequence and no key is eligible
- * across sequences.
+ * no causal row of a square problem is empty).  Grouped-query attention
+ * ("Attention algorithms and data movement", lesson 05): query head h reads
+ * key/value head h / (Hq / Hkv).  Packed variable-length batches (same page,
+ * lesson 04): positions are logical positions inside each sequence and no key
+ * is eligible across sequences.
+ *
+ * The *_ex entry points add unequal query and key lengths (same page, lesson
+ * 04) and local windows (same page, lesson 07).  Query row i of Lq sits at
+ * key position c_i = i + Lk - Lq, so that the last query row aligns with the
+ * last key (a decode step or a chunk of new tokens over a longer cache).  Key
+ * j is eligible for row i iff
+ *     j <= c_i                        (causal)
+ *     c_i - window_left <= j          (window_left  >= 0; negative = no bound)
+ *     j <= c_i + window_right         (window_right >= 0; negative = no bound)
+ * A row with no eligible key (Lk = 0, or Lq > Lk under the causal mask, or a
+ * window past the keys) gets O_i = 0 and lse_i = -inf.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -35,7 +46,9 @@
  *  - Supported: head dim D in {32, 64, 128}; the d-stride of every tensor is
  *    1; all other strides and every base pointer are 16-byte aligned (TMA
  *    rule); scale is finite and > 0.
- *  - Empty work (B, Hq or N equal to 0; or no tokens) is a successful no-op.
+ *  - Empty work (B, Hq or N equal to 0; or no query tokens) is a successful
+ *    no-op.
+ *  - Limits: every length <= 2^30 tokens; B, Hq and num_seqs <= 65535.
  */
 #ifndef ETATTN_H
 #define ETATTN_H
@@ -78,7 +91,6 @@ enum etattn_status {
  *            expressible; the d-stride must be 1.
  *   causal : 0 = every key eligible; 1 = keys j <= i (diagonal included)
  *   scale  : logit scale (commonly 1/sqrt(D))
- * Limits: N <= 8,388,480; B*Hq <= 2^31-1.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
              int D, int dtype, const int64_t* strides, int causal, float scale, void* stream);
@@ -100,11 +112,51 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *            otherwise the kernel checks each sequence it reads and, on a bad
  *            entry, skips that sequence and records ETATTN_ERR_BAD_SEQLENS in
  *            the device status word (see etattn_read_device_status).
- * Limits: max_seqlen <= 8,388,480; num_seqs*Hq <= 2^31-1.
  */
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,
                     const int32_t* cu_seqlens_host, int num_seqs, int max_seqlen, int total_tokens, int Hq,
                     int Hkv, int D, int dtype, const int64_t* strides, int causal, float scale, void* stream);
+
+/*
+ * attn_fwd_ex: attn_fwd with Nq query and Nk key tokens per sequence and an
+ * optional local window (eligibility rule at the top of this file).
+ *
+ *   q, o: logical [B, Hq, Nq, D];  k, v: logical [B, Hkv, Nk, D];
+ *   lse : [B, Hq, Nq] contiguous FP32 (or NULL);  strides as for attn_fwd.
+ *   window_left, window_right: key offsets before / after the row's key
+ *           position; a negative value is no bound.  With causal = 1 the
+ *           right bound is the diagonal whatever window_right says.
+ * Nq = 0 (or B or Hq = 0) is a no-op.  Nk = 0 is valid: every row is empty
+ * and k, v may be NULL.  attn_fwd(..., N, ...) equals
+ * attn_fwd_ex(..., Nq = N, Nk = N, ..., window_left = -1, window_right = -1, ...).
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
+                float scale, void* stream);
+
+/*
+ * attn_fwd_varlen_ex: attn_fwd_varlen with separate packed query and key
+ * offsets and an optional local window.
+ *
+ *   q, o: logical [total_q, Hq, D];  k, v: logical [total_k, Hkv, D];
+ *   lse : [Hq, total_q] contiguous FP32 (or NULL);  strides as for
+ *         attn_fwd_varlen (12 values, (t, h, d) for q, k, v, o).
+ *   cu_seqlens_q / cu_seqlens_k: DEVICE int32 [num_seqs + 1]; sequence s
+ *         owns query tokens cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 and key
+ *         tokens cu_seqlens_k[s] .. cu_seqlens_k[s+1]-1 (both required; they
+ *         may be the same array).  Each must rise from 0 to its total with
+ *         every length <= max_seqlen_q / max_seqlen_k.
+ *   cu_seqlens_q_host / cu_seqlens_k_host: optional HOST mirrors, each
+ *         validated before launch when given (ETATTN_ERR_BAD_SEQLENS);
+ *         otherwise the kernel checks each sequence as attn_fwd_varlen does.
+ * A sequence with no keys gives O = 0 and lse = -inf on its rows; with
+ * total_k = 0, k and v may be NULL.
+ */
+int attn_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
+                       const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                       int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides, int causal,
+                       int window_left, int window_right, float scale, void* stream);
 
 /*
  * attn_fwd_host: attn_fwd for callers whose q, k, v live in HOST memory and

@@ -20,15 +20,21 @@ def to64(t):
     return t.detach().to("cpu", torch.float32).double().numpy()
 
 
-def run_gpu(inputs, causal, scale=None, stream=None):
+def run_gpu(inputs, causal, scale=None, stream=None, window_left=-1, window_right=-1):
     q, k, v = (inputs[n].cuda() if not inputs[n].is_cuda else inputs[n] for n in ("q", "k", "v"))
+    win = dict(window_left=window_left, window_right=window_right)
     if "cu_seqlens" in inputs:
         cu = inputs["cu_seqlens"]
         lens = (cu[1:] - cu[:-1]).tolist()
+        kw = {}
+        if "cu_seqlens_k" in inputs:
+            cuk = inputs["cu_seqlens_k"]
+            lk = (cuk[1:] - cuk[:-1]).tolist()
+            kw = dict(cu_seqlens_k=cuk.cuda(), max_seqlen_k=max(lk) if lk else 0, cu_seqlens_k_host=cuk)
         o, lse = binding.attention_varlen(q, k, v, cu.cuda(), max(lens) if lens else 0, causal=causal,
-                                          scale=scale, cu_seqlens_host=cu, stream=stream)
+                                          scale=scale, cu_seqlens_host=cu, stream=stream, **kw, **win)
     else:
-        o, lse = binding.attention(q, k, v, causal=causal, scale=scale, stream=stream)
+        o, lse = binding.attention(q, k, v, causal=causal, scale=scale, stream=stream, **win)
     torch.cuda.synchronize()
     return o, lse
 
@@ -58,31 +64,40 @@ def derived_bound(ro, v_absmax, keys, dtype):
     return u * v_absmax + u * np.abs(ro) + sub + 1e-5
 
 
-def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True):
+def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True, window_left=-1, window_right=-1):
     """Compare every output element with the dense oracle.  The stated bounds
     (max|dO| <= 2e-3 FP16 / 1e-2 BF16, max|d lse| <= 1e-3) must hold; for
     shapes outside the five specified workloads (derived_ok) an O element may
-    instead meet the arithmetic bound of derived_bound."""
+    instead meet the arithmetic bound of derived_bound.  Rows with no
+    eligible key must be exact: O = 0 and lse = -inf."""
     q64, k64, v64 = to64(inputs["q"]), to64(inputs["k"]), to64(inputs["v"])
+    win = dict(window_left=window_left, window_right=window_right)
     if "cu_seqlens" in inputs:
         cu = inputs["cu_seqlens"].numpy()
-        ro, rl = oracle.attention_varlen(q64, k64, v64, cu, causal=causal, scale=scale)
+        cuk = inputs["cu_seqlens_k"].numpy() if "cu_seqlens_k" in inputs else cu
+        ro, rl = oracle.attention_varlen(q64, k64, v64, cu, causal=causal, scale=scale, cu_seqlens_k=cuk, **win)
         group = q64.shape[1] // k64.shape[1]
         vmax = np.zeros(ro.shape[:2] + (1,))
         keys = 0
         for s_ in range(len(cu) - 1):
             t0, t1 = int(cu[s_]), int(cu[s_ + 1])
-            if t1 > t0:
-                vm = np.abs(v64[t0:t1]).max(axis=(0, 2))  # per kv head
+            k0, k1 = int(cuk[s_]), int(cuk[s_ + 1])
+            if t1 > t0 and k1 > k0:
+                vm = np.abs(v64[k0:k1]).max(axis=(0, 2))  # per kv head
                 vmax[t0:t1, :, 0] = np.repeat(vm, group)[None, :]
-                keys = max(keys, t1 - t0)
+                keys = max(keys, k1 - k0)
     else:
-        ro, rl = oracle.attention_dense(q64, k64, v64, causal=causal, scale=scale)
+        ro, rl = oracle.attention_dense(q64, k64, v64, causal=causal, scale=scale, **win)
         group = q64.shape[1] // k64.shape[1]
-        vmax = np.repeat(np.abs(v64).max(axis=(2, 3)), group, axis=1)[:, :, None, None]
-        keys = q64.shape[2]
+        vmax = (np.repeat(np.abs(v64).max(axis=(2, 3)), group, axis=1)[:, :, None, None] if v64.size
+                else np.zeros(ro.shape[:2] + (1, 1)))
+        keys = k64.shape[2]
     go, gl = to64(o), to64(lse)
     assert np.all(np.isfinite(go)), "non-finite output"
+    empty = ~np.isfinite(rl)
+    empty_o = empty.T if "cu_seqlens" in inputs else empty  # lse [Hq, T] vs O [T, Hq, D] when packed
+    assert np.array_equal(np.isfinite(gl), ~empty), "rows with no eligible key differ"
+    assert np.all(gl[empty] == -np.inf) and np.all(go[empty_o] == 0.0), "empty rows must give O = 0, lse = -inf"
     err = np.abs(go - ro)
     do = float(err.max()) if go.size else 0.0
     finite = np.isfinite(rl)
@@ -102,7 +117,7 @@ def sample_rows(N, rng, extra=8):
     return sorted(r for r in base if 0 <= r < N)
 
 
-def compare_sampled_batched(inputs, o, lse, causal, scale, dtype, heads, rng):
+def compare_sampled_batched(inputs, o, lse, causal, scale, dtype, heads, rng, window_left=-1, window_right=-1):
     """Compare sampled rows of selected (batch, head) pairs with the oracle
     computed row by row."""
     q, k, v = inputs["q"], inputs["k"], inputs["v"]
@@ -113,7 +128,7 @@ def compare_sampled_batched(inputs, o, lse, causal, scale, dtype, heads, rng):
         rows = sample_rows(N, rng)
         hk = h // group
         ro, rl = oracle.attention_rows(to64(q[b, h]), to64(k[b, hk]), to64(v[b, hk]), rows, causal=causal,
-                                       scale=scale)
+                                       scale=scale, window_left=window_left, window_right=window_right)
         go = to64(o[b, h][rows])
         gl = to64(lse[b, h][rows])
         worst_o = max(worst_o, float(np.max(np.abs(go - ro))))

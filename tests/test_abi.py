@@ -171,3 +171,74 @@ def test_host_entry_points_validate_before_copying():
     assert vh(cu_bad) == 9
     assert vh(cu, Hkv=3) == 4
     assert vh(cu, scale=-1.0) == 8
+
+
+def ex_call(**kw):
+    a = good_args(**kw)
+    Nk = kw.get("Nk", a["N"])
+    st = a["strides"] if "strides" in kw else (contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]) +
+                                               contiguous_strides(a["B"], a["Hkv"], Nk, a["D"]) * 2 +
+                                               contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]))
+    return B.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], Nk, a["D"],
+                         a["dtype"], st, a["causal"], kw.get("wl", -1), kw.get("wr", -1), a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nk=-1), 3), (dict(Nk=2 ** 30 + 1), 3), (dict(N=-1), 3),
+    (dict(k=0), 1), (dict(v=0), 1), (dict(q=0), 1),
+    (dict(k=K + 8), 6), (dict(Hkv=3), 4), (dict(scale=0.0), 8),
+])
+def test_ex_invalid_arguments_rejected(kw, code):
+    assert ex_call(**kw) == code
+
+
+def test_ex_empty_queries_are_a_noop_and_no_keys_needs_no_key_pointers():
+    import torch
+    assert ex_call(N=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    rc = ex_call(Nk=0, k=0, v=0, wl=5)  # valid: every row is empty; needs a device to run
+    assert rc == (12 if not torch.cuda.is_available() else 0)
+
+
+def varlen_ex_call(cu_q_host=None, cu_k_host=None, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=LSE, cuq=0x60000000, cuk=0x60001000, num_seqs=3, mq=50, mk=80, Tq=100, Tk=150,
+             Hq=4, Hkv=2, D=128, dtype=1, causal=1, wl=-1, wr=-1, scale=0.1, stream=0)
+    a.update(kw)
+    st = [a["Hq"] * a["D"], a["D"], 1, a["Hkv"] * a["D"], a["D"], 1, a["Hkv"] * a["D"], a["D"], 1,
+          a["Hq"] * a["D"], a["D"], 1]
+    keep = []
+
+    def host(arr):
+        if arr is None:
+            return 0
+        c = (ctypes.c_int32 * len(arr))(*arr)
+        keep.append(c)
+        return ctypes.addressof(c)
+    return B.attn_fwd_varlen_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cuq"], a["cuk"], host(cu_q_host),
+                                host(cu_k_host), a["num_seqs"], a["mq"], a["mk"], a["Tq"], a["Tk"], a["Hq"], a["Hkv"],
+                                a["D"], a["dtype"], st, a["causal"], a["wl"], a["wr"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("cq,ck,code", [
+    ([0, 30, 60, 100], [0, 80, 80, 150], 0),
+    ([0, 30, 60, 100], [0, 80, 70, 150], 9),   # key offsets decrease
+    ([0, 30, 60, 100], [0, 10, 20, 149], 9),   # key offsets end short of the key total
+    ([0, 30, 60, 100], [0, 90, 100, 150], 9),  # a key length above max_seqlen_k
+    ([0, 60, 60, 100], [0, 80, 80, 150], 9),   # a query length above max_seqlen_q
+])
+def test_varlen_ex_host_offsets_validation(cq, ck, code):
+    import torch
+    rc = varlen_ex_call(cu_q_host=cq, cu_k_host=ck)
+    if code == 0:
+        assert rc == (12 if not torch.cuda.is_available() else 0)
+    else:
+        assert rc == code
+
+
+def test_varlen_ex_argument_errors():
+    assert varlen_ex_call(cuk=0) == 1
+    assert varlen_ex_call(cuq=0) == 1
+    assert varlen_ex_call(cuk=0x60001002) == 6
+    assert varlen_ex_call(mk=-1) == 3
+    assert varlen_ex_call(Tk=-1) == 3
+    assert varlen_ex_call(Tq=0) == 0
+    assert varlen_ex_call(num_seqs=0) == 0
