@@ -8,7 +8,7 @@ H=16, D=128, BF16).  Prints ONE JSON line with throughput in TFLOP/s
 the kernel, an end-to-end number through the host-buffer C entry point, the
 CPU oracle baseline, and per-workload microsecond timings.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the FP64 CPU oracle as reference arm
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of
@@ -36,8 +36,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; µs/call (1 GPU)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-PER_CONFIG = ["c1", "c2_causal", "c2_noncausal", "c2_large_logit", "c3", "c3_bnhd", "c4", "c5",
-              "chunk2048_cache16384_gqa", "window4096_n16384"]
+PER_CONFIG = ["n129_d32_f16_causal", "n512_d64_f16_causal", "n512_d64_f16_noncausal", "n512_d64_f16_causal_qx30",
+              "b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd", "gqa_b2_h32x8_n8192_d128_bf16",
+              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384"]
 
 
 def parse_args():
@@ -46,7 +47,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c5")
+    ap.add_argument("--workload", default="varlen16_h16_d128_bf16")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload microbenchmarks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -247,6 +248,8 @@ def time_e2e(w, inp, dev, stream, K, W, world):
     and copies O and lse back."""
     import torch
     from exact_tiled_attention_19_gb300 import binding
+    if not w.square:
+        return None  # the host-buffer entry points take equal query/key lengths without a window
     pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
     o_h = torch.empty(dev["o"].shape, dtype=w.dtype).pin_memory()
     l_h = torch.empty(dev["lse"].shape, dtype=torch.float32).pin_memory()
@@ -332,14 +335,21 @@ def oracle_sample(w):
         hk = h // (w.Hq // w.Hkv)
         probs.append(tuple(inp[n][0, hh].float().double().numpy() for n, hh in (("q", h), ("k", hk), ("v", hk))))
     desc = f"batch 0, query heads {heads}, all {w.N} rows"
-    flops = 4.0 * w.N * w.N * w.D * len(heads) / (2 if w.causal else 1)
+    flops = head_flops(w) * len(heads)
     return desc, probs, flops
+
+
+def head_flops(w):
+    """The metric's FLOPs of one (sequence, query head) of a batched workload
+    (every one is the same size)."""
+    return w.flops_convention() / (w.B * w.Hq)
 
 
 def run_oracle_problem(prob, w):
     import oracle
     q, k, v = prob
-    return oracle.attention_rows(q, k, v, np.arange(q.shape[0]), causal=w.causal, scale=w.scale)
+    return oracle.attention_rows(q, k, v, np.arange(q.shape[0]), causal=w.causal, scale=w.scale,
+                                 window_left=w.window_left, window_right=w.window_right)
 
 
 def cpu_baseline(w):
@@ -358,9 +368,8 @@ def reference_arm(args, w, world, rank):
     oracle sample (rank 0 only)."""
     if rank != 0:
         return None
-    desc, probs, _ = oracle_sample(w)
-    L = probs[0][0].shape[0]
-    step_flops = 4.0 * L * L * w.D / (2 if w.causal else 1)
+    desc, probs, flops = oracle_sample(w)
+    step_flops = flops / len(probs)  # one head per step; every head of the sample is the same size
     for i in range(args.warmup):
         run_oracle_problem(probs[i % len(probs)], w)
     t0 = time.perf_counter()
@@ -381,12 +390,19 @@ def reference_arm(args, w, world, rank):
 
 
 def workload_config(w, n_gpus):
-    return {"workload": f"{w.name}: {w.description}", "global_batch": w.total_tokens * n_gpus,
-            "seq_len": w.N if w.layout != "varlen" else f"packed, max {max(w.seqlens)}",
-            "heads": f"Hq={w.Hq} Hkv={w.Hkv}", "head_dim": w.D, "causal": w.causal,
-            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
-            "l2": f"inputs larger than L2 ({w.io_bytes() / 1e9:.2f} GB algorithmic bytes per step)"
-            if w.io_bytes() > 200e6 else "warm L2 (inputs smaller than L2)"}
+    cfg = {"workload": f"{w.name}: {w.description}", "global_batch": w.total_tokens * n_gpus,
+           "seq_len": w.N if w.layout != "varlen" else f"packed, max {max(w.seqlens)}",
+           "heads": f"Hq={w.Hq} Hkv={w.Hkv}", "head_dim": w.D, "causal": w.causal,
+           "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+           "l2": f"inputs larger than L2 ({w.io_bytes() / 1e9:.2f} GB algorithmic bytes per step)"
+           if w.io_bytes() > 200e6 else "warm L2 (inputs smaller than L2)"}
+    if w.layout != "varlen" and w.keys != w.N:
+        cfg["key_len"] = w.keys
+    if w.window_left >= 0 or w.window_right >= 0:
+        cfg["window"] = {"left": w.window_left, "right": w.window_right}
+    if not w.square:
+        cfg["flops"] = "exact eligible (query, key) pairs x 4 x D per head"
+    return cfg
 
 
 # ---------------------------------------------------------------- correctness gate and per-workload timing

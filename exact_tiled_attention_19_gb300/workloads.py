@@ -122,31 +122,33 @@ class Workload:
         return (2 * tq * self.Hq * self.D + 2 * tk * self.Hkv * self.D) * esz + tq * self.Hq * 4
 
 
-WORKLOADS = {
-    "c1": Workload("c1", "single head, causal, N=129, D=32, FP16", 1, 1, 1, 129, 32, torch.float16, True),
-    "c2_causal": Workload("c2_causal", "single head, causal, N=512, D=64, FP16", 1, 1, 1, 512, 64,
-                          torch.float16, True),
-    "c2_noncausal": Workload("c2_noncausal", "single head, non-causal, N=512, D=64, FP16", 1, 1, 1, 512, 64,
-                             torch.float16, False),
-    "c2_large_logit": Workload("c2_large_logit", "single head, causal, N=512, D=64, FP16, Q x30", 1, 1, 1,
-                               512, 64, torch.float16, True, q_scale=30.0),
-    "c3": Workload("c3", "B=4, H=16, N=4096, D=128, BF16, causal, [B,H,N,D]", 4, 16, 16, 4096, 128,
-                   torch.bfloat16, True),
-    "c3_bnhd": Workload("c3_bnhd", "B=4, H=16, N=4096, D=128, BF16, causal, [B,N,H,D] strides", 4, 16, 16,
-                        4096, 128, torch.bfloat16, True, layout="bnhd"),
-    "c4": Workload("c4", "GQA B=2, Hq=32, Hkv=8, N=8192, D=128, BF16, causal", 2, 32, 8, 8192, 128,
-                   torch.bfloat16, True),
-    "c5": Workload("c5", "packed varlen, 16 sequences (seed 7), H=16, D=128, BF16, causal", 1, 16, 16,
-                   max(VARLEN_LENGTHS_SEED7), 128, torch.bfloat16, True, layout="varlen",
-                   seqlens=tuple(VARLEN_LENGTHS_SEED7)),
+def _named(name, description, *args, **kw):
+    return name, Workload(name, description, *args, **kw)
+
+
+F16, BF16 = torch.float16, torch.bfloat16
+
+# Workloads by what they are: sizes, layout, dtype and mask.
+WORKLOADS = dict([
+    _named("n129_d32_f16_causal", "single head, causal, N=129, D=32, FP16", 1, 1, 1, 129, 32, F16, True),
+    _named("n512_d64_f16_causal", "single head, causal, N=512, D=64, FP16", 1, 1, 1, 512, 64, F16, True),
+    _named("n512_d64_f16_noncausal", "single head, non-causal, N=512, D=64, FP16", 1, 1, 1, 512, 64, F16, False),
+    _named("n512_d64_f16_causal_qx30", "single head, causal, N=512, D=64, FP16, Q x30", 1, 1, 1, 512, 64, F16, True,
+           q_scale=30.0),
+    _named("b4_h16_n4096_d128_bf16", "B=4, H=16, N=4096, D=128, BF16, causal, [B,H,N,D]", 4, 16, 16, 4096, 128,
+           BF16, True),
+    _named("b4_h16_n4096_d128_bf16_bnhd", "B=4, H=16, N=4096, D=128, BF16, causal, [B,N,H,D] strides", 4, 16, 16,
+           4096, 128, BF16, True, layout="bnhd"),
+    _named("gqa_b2_h32x8_n8192_d128_bf16", "GQA B=2, Hq=32, Hkv=8, N=8192, D=128, BF16, causal", 2, 32, 8, 8192,
+           128, BF16, True),
+    _named("varlen16_h16_d128_bf16", "packed varlen, 16 sequences (seed 7), H=16, D=128, BF16, causal", 1, 16, 16,
+           max(VARLEN_LENGTHS_SEED7), 128, BF16, True, layout="varlen", seqlens=tuple(VARLEN_LENGTHS_SEED7)),
     # Unequal lengths and local windows.
-    "chunk2048_cache16384_gqa": Workload(
-        "chunk2048_cache16384_gqa", "GQA B=2, Hq=32, Hkv=8, 2048 new queries over 16384 keys (bottom-right causal), "
-        "D=128, BF16", 2, 32, 8, 2048, 128, torch.bfloat16, True, Nk=16384),
-    "window4096_n16384": Workload(
-        "window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys (diagonal included), D=128, BF16",
-        2, 16, 16, 16384, 128, torch.bfloat16, True, window_left=4095),
-}
+    _named("chunk2048_cache16384_gqa", "GQA B=2, Hq=32, Hkv=8, 2048 new queries over 16384 keys (bottom-right "
+           "causal), D=128, BF16", 2, 32, 8, 2048, 128, BF16, True, Nk=16384),
+    _named("window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys (diagonal included), D=128, "
+           "BF16", 2, 16, 16, 16384, 128, BF16, True, window_left=4095),
+])
 
 
 def varlen_lengths_from_seed(seed: int = 7, count: int = 16, max_len: int = 16384):

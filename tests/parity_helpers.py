@@ -106,8 +106,8 @@ def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True, window_l
     if do > O_TOL[dtype]:
         bound = derived_bound(ro, vmax, keys, dtype)
         worst = float((err / bound).max())
-        assert derived_ok and worst <= 1.0, (
-            f"max|dO|={do} > {O_TOL[dtype]}" + (f" and the arithmetic bound is exceeded ({worst:.3f}x)" if derived_ok else ""))
+        more = f" and the arithmetic bound is exceeded ({worst:.3f}x)" if derived_ok else ""
+        assert derived_ok and worst <= 1.0, f"max|dO|={do} > {O_TOL[dtype]}" + more
     return do, dl
 
 

@@ -72,7 +72,8 @@ def test_nondefault_scale():
 
 # ---------------------------------------------------------------- the named workloads
 
-@pytest.mark.parametrize("name", ["c1", "c2_causal", "c2_noncausal", "c2_large_logit"])
+@pytest.mark.parametrize("name", ["n129_d32_f16_causal", "n512_d64_f16_causal", "n512_d64_f16_noncausal",
+                                  "n512_d64_f16_causal_qx30"])
 def test_small_workloads_full(name):
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w)
@@ -80,7 +81,8 @@ def test_small_workloads_full(name):
     compare_full(inp, o, lse, w.causal, w.scale, w.dtype, derived_ok=False)
 
 
-@pytest.mark.parametrize("name", ["c3", "c3_bnhd", "c4"])
+@pytest.mark.parametrize("name", ["b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd",
+                                  "gqa_b2_h32x8_n8192_d128_bf16"])
 def test_large_batched_workloads_sampled(name):
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w)
@@ -93,7 +95,7 @@ def test_large_batched_workloads_sampled(name):
 
 
 def test_varlen_workload_sampled():
-    w = W.WORKLOADS["c5"]
+    w = W.WORKLOADS["varlen16_h16_d128_bf16"]
     inp = W.make_inputs(w)
     o, lse = run_gpu(inp, w.causal)
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())

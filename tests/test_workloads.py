@@ -16,12 +16,12 @@ def test_cu_seqlens():
 
 
 def test_small_workload_shapes_and_determinism():
-    a = W.make_inputs("c1")
-    b = W.make_inputs("c1")
+    a = W.make_inputs("n129_d32_f16_causal")
+    b = W.make_inputs("n129_d32_f16_causal")
     assert a["q"].shape == (1, 1, 129, 32) and a["q"].dtype == torch.float16
     assert torch.equal(a["q"], b["q"]) and torch.equal(a["v"], b["v"])
-    big = W.make_inputs("c2_large_logit")
-    base = W.make_inputs("c2_causal")
+    big = W.make_inputs("n512_d64_f16_causal_qx30")
+    base = W.make_inputs("n512_d64_f16_causal")
     assert torch.equal(big["k"], base["k"])
     assert float(big["q"].float().abs().max()) > 20 * float(base["q"].float().abs().max()) * 0.9
 
@@ -35,8 +35,8 @@ def test_transposed_layout_is_same_logical_values():
 
 
 def test_flop_and_byte_conventions():
-    c5 = W.WORKLOADS["c5"]
-    assert abs(c5.flops_convention() - 5.507e12) / 5.507e12 < 1e-3
-    c3 = W.WORKLOADS["c3"]
-    assert c3.flops_convention() == 4 * 4096 ** 2 * 128 * 64 / 2
-    assert c3.io_bytes() == 4 * 4 * 16 * 4096 * 128 * 2 + 4 * 16 * 4096 * 4
+    packed = W.WORKLOADS["varlen16_h16_d128_bf16"]
+    assert abs(packed.flops_convention() - 5.507e12) / 5.507e12 < 1e-3
+    batched = W.WORKLOADS["b4_h16_n4096_d128_bf16"]
+    assert batched.flops_convention() == 4 * 4096 ** 2 * 128 * 64 / 2
+    assert batched.io_bytes() == 4 * 4 * 16 * 4096 * 128 * 2 + 4 * 16 * 4096 * 4
