@@ -38,7 +38,7 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; µs/call (1 GPU)
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PER_CONFIG = ["n129_d32_f16_causal", "n512_d64_f16_causal", "n512_d64_f16_noncausal", "n512_d64_f16_causal_qx30",
               "b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd", "gqa_b2_h32x8_n8192_d128_bf16",
-              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384"]
+              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384", "decode_b8_h32x8_k32768"]
 
 
 def parse_args():
@@ -193,7 +193,19 @@ def device_inputs(w, device):
     else:
         dev["o"] = torch.empty((w.B, w.Hq, w.N, w.D), dtype=w.dtype, device=device)
         dev["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
+    if w.splitkv:
+        from exact_tiled_attention_19_gb300 import binding
+        rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.N, w.keys)
+        assert rc == 0, rc
+        dev["splits"] = n
+        need = binding.attn_fwd_splitkv_workspace_size(w.B, w.Hq, w.N, w.D, n)
+        dev["ws"] = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
     return inp, dev
+
+
+def launches_per_call(w):
+    """Kernels one call launches: the split-KV path adds the merge launch."""
+    return 2 if w.splitkv and w.keys > 0 else 1
 
 
 def make_call(w, dev, stream):
@@ -207,6 +219,11 @@ def make_call(w, dev, stream):
         def call():
             binding.attention_varlen(dev["q"], dev["k"], dev["v"], dev["cu"], max(w.seqlens), causal=w.causal,
                                      scale=w.scale, out=dev["o"], lse=dev["lse"], stream=stream, **kw, **win)
+    elif w.splitkv:
+        def call():
+            binding.attention_splitkv(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale,
+                                      num_splits=dev["splits"], workspace=dev["ws"], out=dev["o"], lse=dev["lse"],
+                                      stream=stream, **win)
     else:
         def call():
             binding.attention(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale, out=dev["o"],
@@ -501,6 +518,9 @@ def per_config_report(stream, device, peaks):
             entry["tflops_graph"] = round(tf, 2)
             entry["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
             entry["achieved_gbs_graph"] = round(w.io_bytes() / (us * 1e-6) / 1e9, 1)
+            entry["frac_of_hbm"] = round(entry["achieved_gbs_graph"] / peaks["hbm_gbs"], 4)
+            if w.splitkv:
+                entry["num_splits"] = dev["splits"]
         out[name] = entry
         del inp, dev
         torch.cuda.empty_cache()
@@ -567,6 +587,25 @@ def main():
 
     if rank != 0:
         return 0
+    if w.memory_bound:
+        gbs = w.io_bytes() / (launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic(w.name),
+                    "peak_source": "HBM copy, measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                    else "HBM copy, fallback",
+                    "algorithmic_bytes_per_launch": w.io_bytes(), "algorithmic_flops_per_launch": flops,
+                    "launch_ms_mean": round(launch_ms, 4),
+                    "note": "a split-KV call is two launches (slices, merge); the time covers both"
+                    if w.splitkv else ""}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "traffic": measured_traffic(w.name),
+                    "peak_source": f"bf16 dense burst, {peak_src} (MEASURED_PEAKS.json)"
+                    if peak_src == "measured" else "bf16 dense burst, fallback",
+                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                    "algorithmic_flops_per_launch": flops, "exact_causal_flops_per_launch": w.flops_exact(),
+                    "algorithmic_bytes_per_launch": w.io_bytes(), "launch_ms_mean": round(launch_ms, 4)}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
@@ -574,15 +613,8 @@ def main():
         "data": "synthetic (seeded N(0,1) Q/K/V; seed-7 packed lengths)", "config": workload_config(w, world),
         "us_per_call": round(total_ms / args.steps * 1e3, 2),
         "frac_of_bf16_peak": round(value / world / peaks["bf16_tflops"], 4),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": measured_traffic(w.name),
-                     "peak_source": f"bf16 dense burst, {peak_src} (MEASURED_PEAKS.json)"
-                     if peak_src == "measured" else "bf16 dense burst, fallback",
-                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                     "algorithmic_flops_per_launch": flops, "exact_causal_flops_per_launch": w.flops_exact(),
-                     "algorithmic_bytes_per_launch": w.io_bytes(), "launch_ms_mean": round(launch_ms, 4)},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+        "roofline": roofline,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_call(w), "clocks": clocks,
         "device_status": status, "per_config": per_cfg,
     }
     print(json.dumps(line), flush=True)

@@ -1,7 +1,8 @@
 """ctypes binding of the C ABI in ``include/etattn.h``.
 
-The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_fwd_varlen``,
-``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
+The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_fwd_splitkv``,
+``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
+``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
 ``etattn_read_device_status`` and ``etattn_version`` have the C names and
 arguments (pointers as ints).  The helpers ``attention`` and
@@ -67,6 +68,13 @@ def load_library(path: str | None = None):
         lib.attn_fwd_ex.restype = _int
         lib.attn_fwd_varlen_ex.argtypes = [_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 3 + [ctypes.c_float, _vp]
         lib.attn_fwd_varlen_ex.restype = _int
+        lib.attn_fwd_splitkv.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _int, _vp,
+                                         ctypes.c_size_t, _vp])
+        lib.attn_fwd_splitkv.restype = _int
+        lib.attn_fwd_splitkv_workspace_size.argtypes = [_int] * 5
+        lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_splitkv_plan.argtypes = [_int] * 4 + [ctypes.POINTER(_int)]
+        lib.attn_fwd_splitkv_plan.restype = _int
         lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                                         _int, _i64p, _int, ctypes.c_float, _vp]
         lib.attn_fwd_varlen.restype = _int
@@ -106,6 +114,26 @@ def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, 
     lib = load_library()
     return lib.attn_fwd_ex(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D, dtype,
                            _strides_arg(strides), causal, window_left, window_right, scale, stream or None)
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                     num_splits, workspace, workspace_bytes, stream):
+    """C ``attn_fwd_splitkv``: pointers as ints (0 for NULL), ``strides`` 16 ints."""
+    lib = load_library()
+    return lib.attn_fwd_splitkv(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D,
+                                dtype, _strides_arg(strides), causal, window_left, window_right, scale, num_splits,
+                                workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits) -> int:
+    return load_library().attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits)
+
+
+def attn_fwd_splitkv_plan(B, Hq, Nq, Nk):
+    """(status, num_splits) for the current device."""
+    out = _int(0)
+    rc = load_library().attn_fwd_splitkv_plan(B, Hq, Nq, Nk, ctypes.byref(out))
+    return rc, out.value
 
 
 def attn_fwd_varlen_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
@@ -225,6 +253,42 @@ def attention(q, k, v, *, causal: bool = True, scale: float | None = None, windo
                              float(scale), _stream_handle(stream))
     if rc != 0:
         raise EtattnError(rc, "attn_fwd" if square else "attn_fwd_ex")
+    return out, lse
+
+
+def attention_splitkv(q, k, v, *, causal: bool = True, scale: float | None = None, window_left: int = -1,
+                      window_right: int = -1, num_splits: int | None = None, workspace=None, out=None, lse=None,
+                      return_lse: bool = True, stream=None):
+    """``attention`` computed with the keys cut into ``num_splits`` slices
+    (default: the library's plan for the current device) and merged by a
+    second launch.  ``workspace`` is a CUDA uint8 tensor of at least
+    ``attn_fwd_splitkv_workspace_size`` bytes (allocated here when None)."""
+    import torch
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        if num_splits is None:
+            rc, num_splits = attn_fwd_splitkv_plan(B, Hq, Nq, Nk)
+            if rc != 0:
+                raise EtattnError(rc, "attn_fwd_splitkv_plan")
+        need = attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
+        if lse is None and return_lse:
+            lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+        strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
+        ws_ptr = workspace.data_ptr() if workspace is not None else 0
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if lse is not None else 0, B, Hq, Hkv, Nq, Nk, D, _dtype_code(q),
+                              strides, 1 if causal else 0, int(window_left), int(window_right), float(scale),
+                              int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise EtattnError(rc, "attn_fwd_splitkv")
     return out, lse
 
 

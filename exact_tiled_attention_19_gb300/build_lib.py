@@ -70,7 +70,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     jobs = [([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, "attn_api.cu"), "-o",
-              os.path.join(BUILD_DIR, "attn_api.o")], "attn_api")]
+              os.path.join(BUILD_DIR, "attn_api.o")], "attn_api"),
+            ([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, "attn_combine.cu"), "-o",
+              os.path.join(BUILD_DIR, "attn_combine.o")], "attn_combine")]
     for d, bf in VARIANTS:
         obj = os.path.join(BUILD_DIR, f"attn_fwd_d{d}_{bf}.o")
         jobs.append(([nvcc, *ARCH, *CFLAGS, f"-DETATTN_INST_D={d}", f"-DETATTN_INST_BF16={bf}", "-c",

@@ -185,13 +185,20 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
 // problem that would not fill the GPU with two-sub-tile CTAs runs one
 // sub-tile per CTA instead.  `general` selects the kernel built for unequal
 // query/key lengths and windows; square window-free calls take the other.
+//
+// In a split-KV launch (p.part_o set) every query block gets p.num_splits
+// CTAs, one per key slice.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, bool general,
                    cudaStream_t s) {
   const bool bf = dtype == ETATTN_BF16;
+  const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
   const int64_t blocks2 = (tokens + 255) / 256;
-  const int nsub = blocks2 * (int64_t)gy * gz < num_sms ? 1 : 2;
-  const dim3 g((unsigned)(nsub == 2 ? blocks2 : (tokens + 127) / 128), gy, gz);
+  // Up to 128 query rows fill one sub-tile: a second one would only idle.
+  const int nsub = (tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
+  const int64_t gx = (nsub == 2 ? blocks2 : (tokens + 127) / 128) * splits;
+  if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const dim3 g((unsigned)gx, gy, gz);
   switch (D) {
     case 32:
       return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, general, s) : launch_fwd_d32_0(q, k, v, p, g, nsub, general, s);
@@ -204,6 +211,43 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
 }
 
 bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 128; }
+
+constexpr int kMaxSplits = 1024;
+constexpr size_t kWorkspaceAlign = 256;
+
+// Split-KV workspace: FP32 partial O (num_splits x rows x D), then, at a
+// 256-byte boundary, FP32 partial lse (num_splits x rows).  0 if it would
+// not fit in size_t.
+size_t splitkv_lse_offset(int64_t rows, int D, int num_splits) {
+  const double bytes = (double)num_splits * (double)rows * D * 4.0;
+  if (bytes > 1e18) return 0;
+  return ((size_t)num_splits * (size_t)rows * (size_t)D * 4 + kWorkspaceAlign - 1) / kWorkspaceAlign *
+         kWorkspaceAlign;
+}
+size_t splitkv_bytes(int64_t rows, int D, int num_splits) {
+  if (num_splits <= 1 || rows <= 0) return 0;
+  const size_t off = splitkv_lse_offset(rows, D, num_splits);
+  if (off == 0) return 0;
+  return off + (size_t)num_splits * (size_t)rows * 4;
+}
+
+// Key slices for a split-KV call on a GPU of num_sms SMs: enough CTAs for
+// about four per SM, each slice at least four 128-key tiles, no empty slice.
+int plan_splits(int64_t units, int64_t key_tiles, int num_sms) {
+  if (units <= 0 || key_tiles < 8 || units >= 2 * (int64_t)num_sms) return 1;
+  int64_t splits = (4 * (int64_t)num_sms + units - 1) / units;
+  splits = std::min<int64_t>(splits, std::max<int64_t>(1, key_tiles / 4));
+  splits = std::min<int64_t>(splits, kMaxSplits);
+  const int64_t per = (key_tiles + splits - 1) / splits;
+  return (int)((key_tiles + per - 1) / per);
+}
+
+// Split-KV arguments of fwd_impl.
+struct SplitArgs {
+  int num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+};
 
 }  // namespace
 }  // namespace etattn
@@ -223,7 +267,7 @@ int window_right_of(int wr, int causal) {
 // Validates every argument; launches only when do_launch is set.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
              int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
-             float scale, void* stream, bool do_launch) {
+             float scale, void* stream, bool do_launch, const SplitArgs* split = nullptr) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
   if (Nq > kMaxTokens || Nk > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
@@ -248,6 +292,22 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   for (const View* t : {&vq, &vk, &vv})
     if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
   if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
+  // Split-KV: slices of the keys, merged by a second launch through the
+  // caller's workspace (unused with one slice or no keys).
+  const int64_t rows = (int64_t)B * Hq * Nq;
+  const bool splitting = split != nullptr && split->num_splits > 1 && has_keys;
+  if (split != nullptr && (split->num_splits < 1 || split->num_splits > kMaxSplits)) return ETATTN_ERR_BAD_SHAPE;
+  if (splitting) {
+    const size_t need = splitkv_bytes(rows, D, split->num_splits);
+    if (need == 0) return ETATTN_ERR_BAD_SHAPE;
+    if (split->workspace == nullptr) return ETATTN_ERR_NULL_PTR;
+    if (reinterpret_cast<uintptr_t>(split->workspace) % kWorkspaceAlign) return ETATTN_ERR_BAD_ALIGN;
+    if (split->workspace_bytes < need) return ETATTN_ERR_BAD_SHAPE;
+    const View vw{split->workspace, 1, {(int64_t)need, 0, 0, 0}, {1, 0, 0, 0}};
+    for (const View* t : {&vq, &vk, &vv, &vo})
+      if (overlaps(vw, 1, *t, 2)) return ETATTN_ERR_ALIAS;
+    if (lse && overlaps(vw, 1, vl, 4)) return ETATTN_ERR_ALIAS;
+  }
   if (!do_launch) return ETATTN_OK;
 
   int dev = 0;
@@ -294,10 +354,38 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   // Equal lengths and no left bound: every row reads key 0, so the square
   // kernel applies whatever the right bound.
-  const bool general = Nq != Nk || p.win_left != kUnboundedWindow;
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, Nq, (unsigned)Hq, (unsigned)B, num_sms, general,
-                         static_cast<cudaStream_t>(stream));
+  bool general = Nq != Nk || p.win_left != kUnboundedWindow;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (splitting) {
+    const int key_tiles = (Nk + 127) / 128;
+    uint8_t* ws = static_cast<uint8_t*>(split->workspace);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(ws + splitkv_lse_offset(rows, D, split->num_splits));
+    p.part_stride = rows;
+    p.num_splits = split->num_splits;
+    p.split_tiles = (key_tiles + split->num_splits - 1) / split->num_splits;
+    general = true;  // a slice can hold no key of a row: the general build guards that
+  }
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, Nq, (unsigned)Hq, (unsigned)B, num_sms, general, st);
   if (e != cudaSuccess) return fail_cuda(e);
+  if (splitting) {
+    CombineParams c{};
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.rows = rows;
+    c.num_splits = p.num_splits;
+    c.o = o;
+    c.lse = lse;
+    c.o_sb = strides[12];
+    c.o_sh = strides[13];
+    c.o_sn = strides[14];
+    c.Hq = Hq;
+    c.Nq = Nq;
+    c.packed = 0;
+    c.total = 0;
+    e = launch_combine(D, dtype == ETATTN_BF16, c, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   return ETATTN_OK;
 }
 
@@ -416,6 +504,30 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 float scale, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
                   stream, true);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left,
+                     int window_right, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  const SplitArgs sa{num_splits, workspace, workspace_bytes};
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                  stream, true, &sa);
+}
+
+size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_splits) {
+  if (B < 0 || Hq < 0 || Nq < 0 || !head_dim_ok(D) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_bytes((int64_t)B * Hq * Nq, D, num_splits);
+}
+
+int attn_fwd_splitkv_plan(int B, int Hq, int Nq, int Nk, int* num_splits) {
+  if (num_splits == nullptr) return ETATTN_ERR_NULL_PTR;
+  if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0) return ETATTN_ERR_BAD_SHAPE;
+  int dev = 0, num_sms = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status, &num_sms)) return rc;
+  *num_splits = plan_splits((int64_t)B * Hq * (((int64_t)Nq + 127) / 128), ((int64_t)Nk + 127) / 128, num_sms);
+  return ETATTN_OK;
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,

@@ -20,6 +20,13 @@
 // the key tiles some of its rows may read, and a row that may read none gets
 // O = 0 and lse = -inf.
 //
+// Split-KV ("Intermediate and advanced extension", workshop row "Split
+// softmax" and "Logic review before implementation"): with part_o set, the
+// CTAs of one query block are spread over num_splits slices of the key tiles,
+// and each writes its rows' partial state (O_s = acc_s / l_s in FP32 and
+// lse_s = scale * m_s + ln l_s, or 0 and -inf for a slice with no eligible
+// key) instead of O; a second launch on the same stream merges the slices.
+//
 // A CTA owns 256 query rows as two sub-tiles (rows [0,128) and [128,256) of
 // the block).  Both read the same K/V tiles from shared memory.
 //
@@ -76,6 +83,11 @@ struct FwdParams {
   int Hq, group;                 // query heads, Hq / Hkv
   int win_left, win_right;       // key j is eligible for a row at key position c iff
                                  // c - win_left <= j <= c + win_right (causal: win_right = 0)
+  float* part_o;                 // split-KV partial outputs, or nullptr: FP32, D per row, row r of
+                                 // slice s at (s * part_stride + r) * D, r the row's lse index
+  float* part_lse;               // split-KV partial lse at s * part_stride + r
+  int64_t part_stride;           // rows per slice (the size of lse)
+  int num_splits, split_tiles;   // key-tile slices; key tiles per slice
   float scale;                   // logit scale
   float scale_log2;              // scale * log2(e)
   int* status;                   // device status word
@@ -155,6 +167,7 @@ struct Unit {
   int kt0, n_tot;                // first key tile streamed, tiles streamed
   int f0, f1;                    // first streamed tile read by sub-tile 0 / 1
   int n0, n1;                    // tiles read by sub-tile 0 / 1 (0 = nothing to read)
+  int split;                     // key-tile slice of a split-KV launch (else 0)
   __device__ __forceinline__ int n(int s) const { return s ? n1 : n0; }
   __device__ __forceinline__ int f(int s) const { return s ? f1 : f0; }
   // Sub-tile s reads streamed tile j.
@@ -371,13 +384,25 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     return reinterpret_cast<uint8_t*>(p.o) +
            2 * ((int64_t)u.b * p.o_sb + (int64_t)u.h * p.o_sh + (int64_t)(u.tok0q + row_pos) * p.o_sn);
   };
-  auto lse_at = [&]() { return p.lse + ((int64_t)u.b * p.lse_sb + (int64_t)u.h * p.lse_sh + u.tok0q + row_pos); };
+  auto lse_index = [&]() { return (int64_t)u.b * p.lse_sb + (int64_t)u.h * p.lse_sh + u.tok0q + row_pos; };
+  auto lse_at = [&]() { return p.lse + lse_index(); };
+  // Split-KV partial row: FP32 O_s and lse_s of this CTA's key slice.
+  auto part_index = [&]() { return (int64_t)u.split * p.part_stride + lse_index(); };
+  auto part_row = [&]() { return p.part_o + part_index() * D; };
+  const bool split_mode = GEN && p.part_o != nullptr;
   if (n == 0) {  // no row of this sub-tile may read a key: O = 0, lse = -inf
     if (valid) {
-      uint8_t* orow = o_row();
+      if (split_mode) {
+        float* prow = part_row();
 #pragma unroll
-      for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c * 2) = make_uint4(0u, 0u, 0u, 0u);
-      if (p.lse != nullptr) *lse_at() = -INFINITY;
+        for (int c = 0; c < D; c += 4) *reinterpret_cast<uint4*>(prow + c) = make_uint4(0u, 0u, 0u, 0u);
+        p.part_lse[part_index()] = -INFINITY;
+      } else {
+        uint8_t* orow = o_row();
+#pragma unroll
+        for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c * 2) = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse != nullptr) *lse_at() = -INFINITY;
+      }
     }
     return;
   }
@@ -515,6 +540,27 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   tc_fence_after();
   const bool nonempty = l_run > 0.f;
   const float inv_l = nonempty ? 1.f / l_run : 0.f;
+  if (split_mode) {
+    float* prow = part_row();
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld_x32(tO + c, o);
+      tmem_ld_wait32(o);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(prow + c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_uint4(__float_as_uint(__uint_as_float(o[4 * i]) * inv_l),
+                              __float_as_uint(__uint_as_float(o[4 * i + 1]) * inv_l),
+                              __float_as_uint(__uint_as_float(o[4 * i + 2]) * inv_l),
+                              __float_as_uint(__uint_as_float(o[4 * i + 3]) * inv_l));
+      }
+    }
+    if (valid)
+      p.part_lse[part_index()] = nonempty ? m_run * p.scale + __logf(l_run) : -INFINITY;
+    return;
+  }
   uint8_t* orow = o_row();
 #pragma unroll
   for (int c = 0; c < D; c += 32) {
@@ -576,13 +622,25 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     u.tok0k = k0;
     u.bcoord = 0;
   }
-  const int block = (int)gridDim.x - 1 - (int)blockIdx.x;
+  // x counts query blocks from the last one; in a split-KV launch the slices
+  // of one block are adjacent.
+  int block = (int)gridDim.x - 1 - (int)blockIdx.x;
+  u.split = 0;
+  if (GEN && p.part_o != nullptr) {
+    u.split = (int)blockIdx.x % p.num_splits;
+    block = (int)(gridDim.x / p.num_splits) - 1 - (int)blockIdx.x / p.num_splits;
+  }
   u.row0 = block * C::BLOCK_M;
   if (u.row0 >= u.Lq) return;  // uniform across the CTA
   u.delta = u.Lk - u.Lq;
   {
-    const int2 r0 = sub_tile_key_tiles(u.row0, u, p, C::BN);
-    const int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + C::BM, u, p, C::BN) : make_int2(0, 0);
+    int2 r0 = sub_tile_key_tiles(u.row0, u, p, C::BN);
+    int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + C::BM, u, p, C::BN) : make_int2(0, 0);
+    if (GEN && p.part_o != nullptr) {  // keep this slice's key tiles
+      const int lo = u.split * p.split_tiles, hi = lo + p.split_tiles;
+      r0 = make_int2(max(r0.x, lo), min(r0.y, hi));
+      r1 = make_int2(max(r1.x, lo), min(r1.y, hi));
+    }
     const bool a0 = r0.y > r0.x, a1 = r1.y > r1.x;
     u.kt0 = a0 ? (a1 ? min(r0.x, r1.x) : r0.x) : (a1 ? r1.x : 0);
     u.n_tot = (a0 || a1) ? max(a0 ? r0.y : 0, a1 ? r1.y : 0) - u.kt0 : 0;

@@ -52,6 +52,7 @@ class Workload:
     seqlens_k: tuple = field(default_factory=tuple)  # packed key lengths; empty = seqlens
     window_left: int = -1         # local window (keys before the row's key position); -1 = none
     window_right: int = -1
+    splitkv: bool = False         # run through the split-KV entry point (few queries, many keys)
 
     @property
     def scale(self) -> float:
@@ -114,6 +115,12 @@ class Workload:
         PV, two flops per multiply-add each)."""
         return 4.0 * self.D * self.eligible_pairs() * self.Hq
 
+    @property
+    def memory_bound(self) -> bool:
+        """Below about 64 FLOP per algorithmic byte the HBM, not the tensor
+        core, bounds the call (the GB300 ridge point is near 280)."""
+        return self.flops_convention() < 64 * self.io_bytes()
+
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes of one call: read Q, K, V once, write O and
         the FP32 logsumexp once."""
@@ -148,6 +155,9 @@ WORKLOADS = dict([
            "causal), D=128, BF16", 2, 32, 8, 2048, 128, BF16, True, Nk=16384),
     _named("window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys (diagonal included), D=128, "
            "BF16", 2, 16, 16, 16384, 128, BF16, True, window_left=4095),
+    # Few queries over many keys: split-KV.
+    _named("decode_b8_h32x8_k32768", "decode step: GQA B=8, Hq=32, Hkv=8, 1 query over 32768 keys, D=128, BF16, "
+           "split-KV", 8, 32, 8, 1, 128, BF16, True, Nk=32768, splitkv=True),
 ])
 
 

@@ -53,6 +53,7 @@
 #ifndef ETATTN_H
 #define ETATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -133,6 +134,46 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                 int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
                 float scale, void* stream);
+
+/*
+ * attn_fwd_splitkv: attn_fwd_ex with the keys cut into num_splits slices that
+ * run as separate CTAs, for few query rows over many keys (a decode step).
+ * "Intermediate and advanced extension", workshop row "Split softmax" and
+ * "Logic review before implementation": a first launch writes every row's
+ * partial state per slice (O_s = acc_s / l_s and lse_s = scale*m_s + ln l_s,
+ * FP32), a second launch on the same stream merges the slices (rescaling the
+ * partial sums to the common maximum) and normalises; no cross-block wait.
+ * The result is the same operation as attn_fwd_ex up to rounding order.
+ *
+ *   q, k, v, o, lse, strides, causal, windows, scale: as for attn_fwd_ex.
+ *   num_splits: 1 .. 1024 key slices of ceil(ceil(Nk/128) / num_splits)
+ *           128-key tiles each (attn_fwd_splitkv_plan suggests one).  With
+ *           num_splits = 1 (or Nk = 0) the call is attn_fwd_ex and the
+ *           workspace is not used (it may be NULL).
+ *   workspace: caller-owned DEVICE scratch, 256-byte aligned, of at least
+ *           attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits)
+ *           bytes, private to this call until the merge launch completes on
+ *           `stream` (two calls in flight must not share one).  It may hold
+ *           anything on entry: every slice writes every row before the merge
+ *           reads it.  It must not overlap q, k, v, o or lse
+ *           (ETATTN_ERR_ALIAS); too small or num_splits out of range is
+ *           ETATTN_ERR_BAD_SHAPE; misaligned is ETATTN_ERR_BAD_ALIGN.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left,
+                     int window_right, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Bytes of workspace attn_fwd_splitkv needs (0 when num_splits <= 1, or for
+ * invalid sizes): num_splits * B*Hq*Nq * (4*D + 4) plus alignment padding. */
+size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_splits);
+
+/* A split count for attn_fwd_splitkv on the current device: enough CTAs for
+ * about four per SM when B*Hq*ceil(Nq/128) alone does not fill the GPU, each
+ * slice at least four key tiles; 1 when splitting would not help.  Returns
+ * ETATTN_OK, ETATTN_ERR_NULL_PTR, ETATTN_ERR_BAD_SHAPE or
+ * ETATTN_ERR_NO_DEVICE. */
+int attn_fwd_splitkv_plan(int B, int Hq, int Nq, int Nk, int* num_splits);
 
 /*
  * attn_fwd_varlen_ex: attn_fwd_varlen with separate packed query and key

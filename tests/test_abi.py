@@ -242,3 +242,42 @@ def test_varlen_ex_argument_errors():
     assert varlen_ex_call(Tk=-1) == 3
     assert varlen_ex_call(Tq=0) == 0
     assert varlen_ex_call(num_seqs=0) == 0
+
+
+def test_splitkv_workspace_size_formula():
+    rows = 2 * 8 * 3
+    o_bytes = 5 * rows * 128 * 4
+    padded = (o_bytes + 255) // 256 * 256
+    assert B.attn_fwd_splitkv_workspace_size(2, 8, 3, 128, 5) == padded + 5 * rows * 4
+    assert B.attn_fwd_splitkv_workspace_size(2, 8, 3, 128, 1) == 0
+    assert B.attn_fwd_splitkv_workspace_size(2, 8, 3, 96, 5) == 0      # bad head dim
+    assert B.attn_fwd_splitkv_workspace_size(2, 8, 3, 64, 1025) == 0   # too many slices
+
+
+def splitkv_call(num_splits=4, ws=0x70000000, ws_bytes=1 << 30, **kw):
+    a = good_args(**kw)
+    Nk = kw.get("Nk", a["N"])
+    st = (contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]) + contiguous_strides(a["B"], a["Hkv"], Nk, a["D"]) * 2
+          + contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]))
+    return B.attn_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], Nk, a["D"],
+                              a["dtype"], st, a["causal"], -1, -1, a["scale"], num_splits, ws, ws_bytes, a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_splits=0), 3), (dict(num_splits=1025), 3),
+    (dict(ws=0), 1), (dict(ws=0x70000010), 6), (dict(ws_bytes=1000), 3),
+    (dict(ws=Q), 7), (dict(ws=O - 256), 7),
+    (dict(Hkv=3), 4), (dict(N=-1), 3),
+])
+def test_splitkv_invalid_arguments_rejected(kw, code):
+    assert splitkv_call(**kw) == code
+
+
+def test_splitkv_valid_calls_need_a_device():
+    import torch
+    want = 12 if not torch.cuda.is_available() else 0
+    assert splitkv_call() == want
+    assert splitkv_call(num_splits=1, ws=0, ws_bytes=0) == want   # one slice: no workspace needed
+    assert splitkv_call(N=0) == 0                                 # no queries: no-op
+    rc, n = B.attn_fwd_splitkv_plan(4, 8, 1, 4096)
+    assert rc == want and (rc != 0 or n >= 1)
