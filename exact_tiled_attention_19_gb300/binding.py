@@ -1,6 +1,6 @@
 """ctypes binding of the C ABI in ``include/etattn.h``.
 
-The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_fwd_splitkv``,
+The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_fwd_splitkv``, ``attn_fwd_splitkv_noalloc``,
 ``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
@@ -71,6 +71,9 @@ def load_library(path: str | None = None):
         lib.attn_fwd_splitkv.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _int, _vp,
                                          ctypes.c_size_t, _vp])
         lib.attn_fwd_splitkv.restype = _int
+        lib.attn_fwd_splitkv_noalloc.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 +
+                                                 [ctypes.c_float, _int, _vp])
+        lib.attn_fwd_splitkv_noalloc.restype = _int
         lib.attn_fwd_splitkv_workspace_size.argtypes = [_int] * 5
         lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv_plan.argtypes = [_int] * 4 + [ctypes.POINTER(_int)]
@@ -123,6 +126,16 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, cau
     return lib.attn_fwd_splitkv(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D,
                                 dtype, _strides_arg(strides), causal, window_left, window_right, scale, num_splits,
                                 workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left,
+                             window_right, scale, num_splits, stream):
+    """C ``attn_fwd_splitkv_noalloc``: the split-KV call on the library's
+    fixed 16 MiB scratch (no workspace argument)."""
+    lib = load_library()
+    return lib.attn_fwd_splitkv_noalloc(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk,
+                                        D, dtype, _strides_arg(strides), causal, window_left, window_right, scale,
+                                        num_splits, stream or None)
 
 
 def attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits) -> int:

@@ -25,6 +25,14 @@ namespace etattn {
 // Device status word shared by every launch on a device (0 = ok).
 __device__ int g_status_word;
 
+// Split-KV scratch of attn_fwd_splitkv_noalloc: a fixed, module-owned buffer
+// for callers that cannot hand over device memory (see that entry point).
+// Its size bounds the problems it accepts.  Nothing in it has to start at
+// zero: every key slice writes every row's partial state before the merge
+// launch reads it.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxTokens = 1 << 30;      // token coordinates stay well inside int32
@@ -248,6 +256,32 @@ struct SplitArgs {
   void* workspace;
   size_t workspace_bytes;
 };
+
+// Address of g_splitkv_scratch on the current device, looked up once per
+// device (the first call on a device makes this runtime query).
+std::atomic<void*> g_scratch_addr[64];
+std::mutex g_scratch_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return ETATTN_ERR_NO_DEVICE;
+  }
+  void* addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr == nullptr) {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    addr = g_scratch_addr[dev].load();
+    if (addr == nullptr) {
+      e = cudaGetSymbolAddress(&addr, g_splitkv_scratch);
+      if (e != cudaSuccess || addr == nullptr) return fail_cuda(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+      g_scratch_addr[dev].store(addr, std::memory_order_release);
+    }
+  }
+  *out = addr;
+  return ETATTN_OK;
+}
 
 }  // namespace
 }  // namespace etattn
@@ -511,6 +545,32 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      int window_right, float scale, int num_splits, void* workspace, size_t workspace_bytes,
                      void* stream) {
   const SplitArgs sa{num_splits, workspace, workspace_bytes};
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                  stream, true, &sa);
+}
+
+// For callers that cannot allocate device memory at call time: a runtime
+// whose device memory is all held by its own pool and that offers the
+// attention call no allocation hook, or a plugin that is handed only the
+// tensors of the step.  They get the split-KV path with the library's own
+// fixed scratch instead of a workspace argument.
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal,
+                             int window_left, int window_right, float scale, int num_splits, void* stream) {
+  if (B < 0 || Hq < 0 || Nq < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ETATTN_ERR_BAD_SHAPE;
+  const int64_t rows = (int64_t)B * Hq * Nq;
+  if (num_splits > 1 && rows > 0 &&
+      (splitkv_bytes(rows, D, num_splits) == 0 || splitkv_bytes(rows, D, num_splits) > kNoAllocScratchBytes))
+    return ETATTN_ERR_BAD_SHAPE;  // beyond the fixed scratch
+  // Every other argument is checked before the first device query.
+  if (int rc = fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right,
+                        scale, stream, false))
+    return rc;
+  if (B == 0 || Hq == 0 || Nq == 0) return ETATTN_OK;
+  void* scratch = nullptr;
+  if (int rc = noalloc_scratch(&scratch)) return rc;
+  const SplitArgs sa{num_splits, scratch, kNoAllocScratchBytes};
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
                   stream, true, &sa);
 }

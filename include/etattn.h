@@ -176,6 +176,31 @@ size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_spl
 int attn_fwd_splitkv_plan(int B, int Hq, int Nq, int Nk, int* num_splits);
 
 /*
+ * attn_fwd_splitkv_noalloc: attn_fwd_splitkv without a workspace argument,
+ * for callers that cannot allocate device memory at call time (a runtime
+ * whose device memory all belongs to its own pool with no allocation hook for
+ * this call, or a plugin handed only the step's tensors).  The pages have no
+ * counterpart of this entry point.
+ *
+ * The partial states go to one scratch buffer of 16 MiB that the library
+ * owns for each device (a statically sized device array; no allocation at any
+ * call).  A problem whose attn_fwd_splitkv_workspace_size(B, Hq, Nq, D,
+ * num_splits) exceeds 16 MiB is refused with ETATTN_ERR_BAD_SHAPE before any
+ * device work; num_splits = 1 (or Nk = 0) needs no scratch.  Nothing in the
+ * scratch has to start at zero.  Because the buffer is shared, two calls on
+ * one device must not overlap in time: calls on one stream are ordered, but
+ * calls on different streams, or from different host threads, without an
+ * ordering between them race on the scratch and may return wrong results.
+ * The first call on each device looks up the buffer's address (a CUDA
+ * runtime query) and sets kernel attributes; make that first call before any
+ * stream capture begins.  Other arguments, results and errors are those of
+ * attn_fwd_splitkv.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal,
+                             int window_left, int window_right, float scale, int num_splits, void* stream);
+
+/*
  * attn_fwd_varlen_ex: attn_fwd_varlen with separate packed query and key
  * offsets and an optional local window.
  *

@@ -281,3 +281,24 @@ def test_splitkv_valid_calls_need_a_device():
     assert splitkv_call(N=0) == 0                                 # no queries: no-op
     rc, n = B.attn_fwd_splitkv_plan(4, 8, 1, 4096)
     assert rc == want and (rc != 0 or n >= 1)
+
+
+def noalloc_call(num_splits=4, **kw):
+    a = good_args(**kw)
+    Nk = kw.get("Nk", a["N"])
+    st = (contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]) + contiguous_strides(a["B"], a["Hkv"], Nk, a["D"]) * 2
+          + contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]))
+    return B.attn_fwd_splitkv_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], Nk,
+                                      a["D"], a["dtype"], st, a["causal"], -1, -1, a["scale"], num_splits,
+                                      a["stream"])
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch_before_any_device_work():
+    import torch
+    # 2 x 4 x 100 rows x 64 slices x (4 * 64 + 4) bytes = 13.3 MB fits in 16 MiB; 128 slices do not.
+    want = 12 if not torch.cuda.is_available() else 0
+    assert noalloc_call(num_splits=64) == want
+    assert noalloc_call(num_splits=128) == 3
+    assert noalloc_call(num_splits=0) == 3
+    assert noalloc_call(num_splits=4, o=Q + 64) == 7
+    assert noalloc_call(num_splits=4, N=0) == 0
