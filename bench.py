@@ -195,7 +195,7 @@ def device_inputs(w, device):
         dev["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
     if w.splitkv:
         from exact_tiled_attention_19_gb300 import binding
-        rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.N, w.keys)
+        rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.Hkv, w.N, w.keys)
         assert rc == 0, rc
         dev["splits"] = n
         need = binding.attn_fwd_splitkv_workspace_size(w.B, w.Hq, w.N, w.D, n)

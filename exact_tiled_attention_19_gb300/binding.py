@@ -76,7 +76,7 @@ def load_library(path: str | None = None):
         lib.attn_fwd_splitkv_noalloc.restype = _int
         lib.attn_fwd_splitkv_workspace_size.argtypes = [_int] * 5
         lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
-        lib.attn_fwd_splitkv_plan.argtypes = [_int] * 4 + [ctypes.POINTER(_int)]
+        lib.attn_fwd_splitkv_plan.argtypes = [_int] * 5 + [ctypes.POINTER(_int)]
         lib.attn_fwd_splitkv_plan.restype = _int
         lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                                         _int, _i64p, _int, ctypes.c_float, _vp]
@@ -142,10 +142,10 @@ def attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits) -> int:
     return load_library().attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits)
 
 
-def attn_fwd_splitkv_plan(B, Hq, Nq, Nk):
+def attn_fwd_splitkv_plan(B, Hq, Hkv, Nq, Nk):
     """(status, num_splits) for the current device."""
     out = _int(0)
-    rc = load_library().attn_fwd_splitkv_plan(B, Hq, Nq, Nk, ctypes.byref(out))
+    rc = load_library().attn_fwd_splitkv_plan(B, Hq, Hkv, Nq, Nk, ctypes.byref(out))
     return rc, out.value
 
 
@@ -283,7 +283,7 @@ def attention_splitkv(q, k, v, *, causal: bool = True, scale: float | None = Non
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
         if num_splits is None:
-            rc, num_splits = attn_fwd_splitkv_plan(B, Hq, Nq, Nk)
+            rc, num_splits = attn_fwd_splitkv_plan(B, Hq, Hkv, Nq, Nk)
             if rc != 0:
                 raise EtattnError(rc, "attn_fwd_splitkv_plan")
         need = attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, num_splits)

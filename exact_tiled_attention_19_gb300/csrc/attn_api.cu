@@ -156,10 +156,12 @@ int current_device(int* dev_out, int** status_out, int* num_sms_out = nullptr) {
 }
 
 // 4-D tensor map over (d, token, head, batch) with a box of one 128-row tile
-// of SW elements along d.  If the token stride exceeds the head stride the
-// two middle axes are exchanged so that strides grow outward; *swapped says so.
+// of SW elements along d: 128 tokens of one head, or with box_heads = P > 1,
+// 128 / P tokens of P heads.  If the token stride exceeds the head stride
+// the two middle axes are exchanged so that strides grow outward; *swapped
+// says so.
 int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_tokens, int64_t n_heads,
-               int64_t n_batch, int64_t s_tok, int64_t s_head, int64_t s_batch, bool* swapped) {
+               int64_t n_batch, int64_t s_tok, int64_t s_head, int64_t s_batch, bool* swapped, int box_heads = 1) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail_cuda(cudaErrorNotSupported);
   const uint64_t esz = 2;
@@ -177,7 +179,8 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)(sw ? n_heads : n_tokens), (cuuint64_t)(sw ? n_tokens : n_heads),
                         (cuuint64_t)n_batch};
   cuuint64_t strides[3] = {sw ? bh : bt, sw ? bt : bh, bb};
-  cuuint32_t box[4] = {(cuuint32_t)sw_elems, sw ? 1u : 128u, sw ? 128u : 1u, 1u};
+  const cuuint32_t box_tok = 128u / (cuuint32_t)box_heads, box_head = (cuuint32_t)box_heads;
+  cuuint32_t box[4] = {(cuuint32_t)sw_elems, sw ? box_head : box_tok, sw ? box_tok : box_head, 1u};
   cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = enc(map, dtype == ETATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                    const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -196,6 +199,9 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
 //
 // In a split-KV launch (p.part_o set) every query block gets p.num_splits
 // CTAs, one per key slice.
+//
+// With grouped-query packing (p.qpack = P > 1) `tokens` counts rows (query
+// tokens x P) and gy head packs; such launches use one sub-tile per CTA.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, bool general,
                    cudaStream_t s) {
@@ -203,7 +209,7 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
   const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
   const int64_t blocks2 = (tokens + 255) / 256;
   // Up to 128 query rows fill one sub-tile: a second one would only idle.
-  const int nsub = (tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
+  const int nsub = (p.qpack > 1 || tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
   const int64_t gx = (nsub == 2 ? blocks2 : (tokens + 127) / 128) * splits;
   if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const dim3 g((unsigned)gx, gy, gz);
@@ -221,6 +227,16 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
 bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 128; }
 
 constexpr int kMaxSplits = 1024;
+
+// Query heads packed into one 128-row tile: the largest power of two that
+// divides the group size, when the general build runs fewer than 128 query
+// tokens per sequence (so that a tile would otherwise stay mostly empty).
+int qpack_of(bool general, int group, int64_t q_tokens) {
+  if (!general || group <= 1 || q_tokens >= 128) return 1;
+  int P = 1;
+  while (P < 128 && group % (2 * P) == 0) P *= 2;
+  return P;
+}
 constexpr size_t kWorkspaceAlign = 256;
 
 // Split-KV workspace: FP32 partial O (num_splits x rows x D), then, at a
@@ -239,8 +255,9 @@ size_t splitkv_bytes(int64_t rows, int D, int num_splits) {
   return off + (size_t)num_splits * (size_t)rows * 4;
 }
 
-// Key slices for a split-KV call on a GPU of num_sms SMs: enough CTAs for
-// about four per SM, each slice at least four 128-key tiles, no empty slice.
+// Key slices for a split-KV call on a GPU of num_sms SMs, given the CTAs of
+// one slice (units): enough CTAs for about four per SM, each slice at least
+// four 128-key tiles, no empty slice.
 int plan_splits(int64_t units, int64_t key_tiles, int num_sms) {
   if (units <= 0 || key_tiles < 8 || units >= 2 * (int64_t)num_sms) return 1;
   int64_t splits = (4 * (int64_t)num_sms + units - 1) / units;
@@ -349,9 +366,15 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   int num_sms = 0;
   if (int rc = current_device(&dev, &status, &num_sms)) return rc;
 
+  // Equal lengths and no left bound: every row reads key 0, so the square
+  // kernel applies whatever the right bound.  A split-KV slice can hold no
+  // key of a row: the general build guards that.
+  const bool general = Nq != Nk || window_left_of(window_left) != kUnboundedWindow || splitting;
+  const int qpack = qpack_of(general, Hq / Hkv, Nq);
+
   CUtensorMap mq, mk, mv;
   bool swq = false, swk = false, swv = false;
-  if (int rc = encode_map(&mq, dtype, q, D, Nq, Hq, B, strides[2], strides[1], strides[0], &swq)) return rc;
+  if (int rc = encode_map(&mq, dtype, q, D, Nq, Hq, B, strides[2], strides[1], strides[0], &swq, qpack)) return rc;
   if (has_keys) {
     if (int rc = encode_map(&mk, dtype, k, D, Nk, Hkv, B, strides[6], strides[5], strides[4], &swk)) return rc;
     if (int rc = encode_map(&mv, dtype, v, D, Nk, Hkv, B, strides[10], strides[9], strides[8], &swv)) return rc;
@@ -386,9 +409,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  // Equal lengths and no left bound: every row reads key 0, so the square
-  // kernel applies whatever the right bound.
-  bool general = Nq != Nk || p.win_left != kUnboundedWindow;
+  p.qpack = qpack;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (splitting) {
     const int key_tiles = (Nk + 127) / 128;
@@ -398,9 +419,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.part_stride = rows;
     p.num_splits = split->num_splits;
     p.split_tiles = (key_tiles + split->num_splits - 1) / split->num_splits;
-    general = true;  // a slice can hold no key of a row: the general build guards that
   }
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, Nq, (unsigned)Hq, (unsigned)B, num_sms, general, st);
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)Nq * qpack, (unsigned)(Hq / qpack), (unsigned)B, num_sms,
+                         general, st);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splitting) {
     CombineParams c{};
@@ -480,9 +501,14 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   int num_sms = 0;
   if (int rc = current_device(&dev, &status, &num_sms)) return rc;
 
+  // Shared query and key offsets mean equal lengths in every sequence (see
+  // fwd_impl for why the right bound does not matter).
+  const bool general = cu_seqlens_k != cu_seqlens_q || window_left_of(window_left) != kUnboundedWindow;
+  const int qpack = qpack_of(general, Hq / Hkv, max_seqlen_q);
+
   CUtensorMap mq, mk, mv;
   bool swq = false, swk = false, swv = false;
-  if (int rc = encode_map(&mq, dtype, q, D, T, Hq, 1, strides[0], strides[1], 0, &swq)) return rc;
+  if (int rc = encode_map(&mq, dtype, q, D, T, Hq, 1, strides[0], strides[1], 0, &swq, qpack)) return rc;
   if (has_keys) {
     if (int rc = encode_map(&mk, dtype, k, D, Tk, Hkv, 1, strides[3], strides[4], 0, &swk)) return rc;
     if (int rc = encode_map(&mv, dtype, v, D, Tk, Hkv, 1, strides[6], strides[7], 0, &swv)) return rc;
@@ -515,11 +541,9 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
-  // Shared query and key offsets mean equal lengths in every sequence (see
-  // fwd_impl for why the right bound does not matter).
-  const bool general = cu_seqlens_k != cu_seqlens_q || p.win_left != kUnboundedWindow;
-  cudaError_t e = launch(D, dtype, mq, mk, mv, p, max_seqlen_q, (unsigned)Hq, (unsigned)num_seqs, num_sms, general,
-                         static_cast<cudaStream_t>(stream));
+  p.qpack = qpack;
+  cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)max_seqlen_q * qpack, (unsigned)(Hq / qpack),
+                         (unsigned)num_seqs, num_sms, general, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }
@@ -580,13 +604,16 @@ size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_spl
   return splitkv_bytes((int64_t)B * Hq * Nq, D, num_splits);
 }
 
-int attn_fwd_splitkv_plan(int B, int Hq, int Nq, int Nk, int* num_splits) {
+int attn_fwd_splitkv_plan(int B, int Hq, int Hkv, int Nq, int Nk, int* num_splits) {
   if (num_splits == nullptr) return ETATTN_ERR_NULL_PTR;
   if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0) return ETATTN_ERR_BAD_SHAPE;
+  if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   int dev = 0, num_sms = 0;
   int* status = nullptr;
   if (int rc = current_device(&dev, &status, &num_sms)) return rc;
-  *num_splits = plan_splits((int64_t)B * Hq * (((int64_t)Nq + 127) / 128), ((int64_t)Nk + 127) / 128, num_sms);
+  const int P = qpack_of(true, Hq / Hkv, Nq);  // split launches use the general build
+  const int64_t units = (int64_t)B * (Hq / P) * (((int64_t)Nq * P + 127) / 128);
+  *num_splits = plan_splits(units, ((int64_t)Nk + 127) / 128, num_sms);
   return ETATTN_OK;
 }
 

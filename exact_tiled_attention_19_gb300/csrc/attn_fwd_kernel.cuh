@@ -27,6 +27,12 @@
 // lse_s = scale * m_s + ln l_s, or 0 and -inf for a slice with no eligible
 // key) instead of O; a second launch on the same stream merges the slices.
 //
+// Grouped-query packing (general build): with qpack = P > 1, a 128-row
+// sub-tile holds 128 / P query tokens of each of P query heads that share one
+// key/value head ("Attention algorithms and data movement", lesson 05), so a
+// few-query call (a decode step) streams each K/V tile once for the group and
+// fills P times more of the tile.
+//
 // A CTA owns 256 query rows as two sub-tiles (rows [0,128) and [128,256) of
 // the block).  Both read the same K/V tiles from shared memory.
 //
@@ -88,6 +94,7 @@ struct FwdParams {
   float* part_lse;               // split-KV partial lse at s * part_stride + r
   int64_t part_stride;           // rows per slice (the size of lse)
   int num_splits, split_tiles;   // key-tile slices; key tiles per slice
+  int qpack;                     // query heads per 128-row sub-tile (1, or a power of two dividing group)
   float scale;                   // logit scale
   float scale_log2;              // scale * log2(e)
   int* status;                   // device status word
@@ -159,7 +166,8 @@ struct SmemBarriers {
 // the order kt0, kt0 + 1, ..., kt0 + n_tot - 1; sub-tile s reads streamed
 // tiles f_s .. f_s + n_s - 1 of them (the two ranges overlap or touch).
 struct Unit {
-  int h, hk, b, bcoord;          // query head, kv head, batch/sequence index, batch coordinate of the maps
+  int h, hk, b, bcoord;          // (first) query head, kv head, batch/sequence index, batch coordinate of the maps
+  int P, span;                   // query heads per sub-tile, query tokens per sub-tile (P * span = 128)
   int tok0q, tok0k;              // first query / key token of the sequence (packed batch), else 0
   int Lq, Lk;                    // query / key length of the sequence
   int delta;                     // Lk - Lq: query row r sits at key position r + delta
@@ -174,11 +182,11 @@ struct Unit {
   __device__ __forceinline__ bool reads(int s, int j) const { return (unsigned)(j - f(s)) < (unsigned)n(s); }
 };
 
-// Key tiles [first, end) that some row of the query rows [r0, r0 + 128)
+// Key tiles [first, end) that some row of the query tokens [r0, r0 + span)
 // (clipped to the sequence) may read; {0, 0} when none may read any key.
-__device__ __forceinline__ int2 sub_tile_key_tiles(int r0, const Unit& u, const FwdParams& p, int bn) {
+__device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit& u, const FwdParams& p, int bn) {
   if (r0 >= u.Lq) return make_int2(0, 0);
-  const int c_first = r0 + u.delta, c_last = min(r0 + 127, u.Lq - 1) + u.delta;
+  const int c_first = r0 + u.delta, c_last = min(r0 + span - 1, u.Lq - 1) + u.delta;
   const int lo = max(0, c_first - p.win_left), hi = min(u.Lk - 1, c_last + p.win_right);
   if (hi < lo) return make_int2(0, 0);
   return make_int2(lo / bn, hi / bn + 1);
@@ -201,7 +209,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_Q + s * C::Q_BYTES + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full,
-                      c * C::SW_ELEMS, u.tok0q + u.row0 + s * C::BM, u.h, u.bcoord, swq);
+                      c * C::SW_ELEMS, u.tok0q + u.row0 + s * u.span, u.h, u.bcoord, swq);
   }
   int ks = 0, kph = 0;  // K ring slot and its phase for tile j
   for (int j = 0; j < u.n_tot; ++j) {
@@ -375,16 +383,30 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   using C = TileCfg<D, NSUB>;
   constexpr uint32_t FULL = 0xffffffffu;
   const int n = u.n(s);
-  const int t = threadIdx.x & 127;  // query row inside the sub-tile = tensor-memory lane
-  const int row_pos = u.row0 + s * C::BM + t;  // logical position inside the query sequence
+  const int t = threadIdx.x & 127;  // row inside the sub-tile = tensor-memory lane
+  // Row t holds query head u.h + hl at token tl of the sub-tile.  A packed Q
+  // box is laid out head-major ((d, token, head) maps) or token-major
+  // ((d, head, token) maps).
+  int hl = 0, tl = t;
+  if (GEN && u.P > 1) {
+    if (p.hn_swapped & 1) {
+      hl = t & (u.P - 1);
+      tl = t / u.P;
+    } else {
+      hl = t / u.span;
+      tl = t & (u.span - 1);
+    }
+  }
+  const int head = u.h + hl;
+  const int row_pos = u.row0 + s * u.span + tl;  // logical position inside the query sequence
   const bool valid = row_pos < u.Lq;
   // Output row and lse addresses (formed where they are used, so that they
   // hold no registers across the tile loop).
   auto o_row = [&]() {
     return reinterpret_cast<uint8_t*>(p.o) +
-           2 * ((int64_t)u.b * p.o_sb + (int64_t)u.h * p.o_sh + (int64_t)(u.tok0q + row_pos) * p.o_sn);
+           2 * ((int64_t)u.b * p.o_sb + (int64_t)head * p.o_sh + (int64_t)(u.tok0q + row_pos) * p.o_sn);
   };
-  auto lse_index = [&]() { return (int64_t)u.b * p.lse_sb + (int64_t)u.h * p.lse_sh + u.tok0q + row_pos; };
+  auto lse_index = [&]() { return (int64_t)u.b * p.lse_sb + (int64_t)head * p.lse_sh + u.tok0q + row_pos; };
   auto lse_at = [&]() { return p.lse + lse_index(); };
   // Split-KV partial row: FP32 O_s and lse_s of this CTA's key slice.
   auto part_index = [&]() { return (int64_t)u.split * p.part_stride + lse_index(); };
@@ -601,7 +623,9 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   Unit u;
-  u.h = blockIdx.y;
+  u.P = GEN ? p.qpack : 1;
+  u.span = C::BM / u.P;
+  u.h = blockIdx.y * u.P;
   u.b = blockIdx.z;
   u.hk = u.h / p.group;
   u.Lq = p.Nq;
@@ -630,12 +654,12 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     u.split = (int)blockIdx.x % p.num_splits;
     block = (int)(gridDim.x / p.num_splits) - 1 - (int)blockIdx.x / p.num_splits;
   }
-  u.row0 = block * C::BLOCK_M;
+  u.row0 = block * NSUB * u.span;
   if (u.row0 >= u.Lq) return;  // uniform across the CTA
   u.delta = u.Lk - u.Lq;
   {
-    int2 r0 = sub_tile_key_tiles(u.row0, u, p, C::BN);
-    int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + C::BM, u, p, C::BN) : make_int2(0, 0);
+    int2 r0 = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN);
+    int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + u.span, u.span, u, p, C::BN) : make_int2(0, 0);
     if (GEN && p.part_o != nullptr) {  // keep this slice's key tiles
       const int lo = u.split * p.split_tiles, hi = lo + p.split_tiles;
       r0 = make_int2(max(r0.x, lo), min(r0.y, hi));

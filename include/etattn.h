@@ -169,11 +169,13 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
 size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_splits);
 
 /* A split count for attn_fwd_splitkv on the current device: enough CTAs for
- * about four per SM when B*Hq*ceil(Nq/128) alone does not fill the GPU, each
- * slice at least four key tiles; 1 when splitting would not help.  Returns
- * ETATTN_OK, ETATTN_ERR_NULL_PTR, ETATTN_ERR_BAD_SHAPE or
- * ETATTN_ERR_NO_DEVICE. */
-int attn_fwd_splitkv_plan(int B, int Hq, int Nq, int Nk, int* num_splits);
+ * about four per SM when the query tiles alone do not fill the GPU, each
+ * slice at least four key tiles; 1 when splitting would not help.  (Fewer
+ * than 128 query tokens of a grouped-query problem share a 128-row tile
+ * among up to Hq/Hkv query heads, so Hkv enters the count.)  Returns
+ * ETATTN_OK, ETATTN_ERR_NULL_PTR, ETATTN_ERR_BAD_SHAPE, ETATTN_ERR_BAD_HEADS
+ * or ETATTN_ERR_NO_DEVICE. */
+int attn_fwd_splitkv_plan(int B, int Hq, int Hkv, int Nq, int Nk, int* num_splits);
 
 /*
  * attn_fwd_splitkv_noalloc: attn_fwd_splitkv without a workspace argument,

@@ -279,7 +279,7 @@ def test_splitkv_valid_calls_need_a_device():
     assert splitkv_call() == want
     assert splitkv_call(num_splits=1, ws=0, ws_bytes=0) == want   # one slice: no workspace needed
     assert splitkv_call(N=0) == 0                                 # no queries: no-op
-    rc, n = B.attn_fwd_splitkv_plan(4, 8, 1, 4096)
+    rc, n = B.attn_fwd_splitkv_plan(4, 8, 2, 1, 4096)
     assert rc == want and (rc != 0 or n >= 1)
 
 

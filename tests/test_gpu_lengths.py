@@ -155,3 +155,32 @@ def test_named_length_and_window_workloads_sampled(name):
     heads = [(0, 0), (w.B - 1, w.Hq - 1), (1 % w.B, w.Hq // 2), (0, 5 % w.Hq)]
     compare_sampled_batched(inp, o.cpu(), lse.cpu(), w.causal, w.scale, w.dtype, heads, rng,
                             window_left=w.window_left, window_right=w.window_right)
+
+
+# ---------------------------------------------------------------- grouped-query packing
+# Fewer than 128 query tokens of a grouped-query problem share a 128-row tile
+# among P query heads of one KV group (P = the largest power of two dividing
+# Hq / Hkv): 128 / P tokens of each head.
+
+@pytest.mark.parametrize("Hq,Hkv", [(12, 2), (16, 1), (64, 1), (128, 1)])
+@pytest.mark.parametrize("Nq", [1, 3, 40])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+def test_gqa_packing_group_sizes(Hq, Hkv, Nq, layout):
+    inp = W.random_qkv(2, Hq, Hkv, Nq, 64, torch.float16, seed=Hq + Nq, layout=layout, Nk=700)
+    dev = {k_: rebuild_strided(t) for k_, t in inp.items()}
+    o, lse = run_gpu(dev, True)
+    compare_full(inp, o, lse, True, default_scale(64), torch.float16)
+
+
+def test_gqa_packing_with_window_and_empty_rows():
+    inp = W.random_qkv(1, 8, 2, 100, 128, torch.bfloat16, seed=31, Nk=60)  # first 40 causal rows empty
+    o, lse = run_gpu(inp, True, window_left=20)
+    compare_full(inp, o, lse, True, default_scale(128), torch.bfloat16, window_left=20)
+
+
+def test_gqa_packing_packed_batch():
+    lq = [1, 5, 0, 64, 2]
+    lk = [300, 700, 10, 64, 0]
+    inp = W.random_varlen(lq, 8, 2, 128, torch.bfloat16, seed=29, lengths_k=lk)
+    o, lse = run_gpu(inp, True)
+    compare_full(inp, o, lse, True, default_scale(128), torch.bfloat16)

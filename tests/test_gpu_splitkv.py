@@ -108,18 +108,19 @@ def test_split_and_plain_results_agree_within_rounding():
 
 
 def test_plan_is_sane():
-    rc, n = binding.attn_fwd_splitkv_plan(8, 32, 1, 32768)
+    rc, n = binding.attn_fwd_splitkv_plan(8, 32, 8, 1, 32768)
     assert rc == 0 and 2 <= n <= 64
-    rc, n = binding.attn_fwd_splitkv_plan(4, 16, 4096, 4096)
+    rc, n = binding.attn_fwd_splitkv_plan(4, 16, 16, 4096, 4096)
     assert rc == 0 and n == 1  # enough query blocks to fill the GPU
-    rc, n = binding.attn_fwd_splitkv_plan(1, 1, 1, 500)
+    rc, n = binding.attn_fwd_splitkv_plan(1, 1, 1, 1, 500)
     assert rc == 0 and n == 1  # too few key tiles to cut
+    assert binding.attn_fwd_splitkv_plan(1, 6, 4, 1, 500)[0] == 4  # Hq not a multiple of Hkv
 
 
 def test_named_decode_workload():
     w = W.WORKLOADS["decode_b8_h32x8_k32768"]
     inp = W.make_inputs(w)
-    rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.N, w.keys)
+    rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.Hkv, w.N, w.keys)
     assert rc == 0 and n > 1
     o, lse = run_split(inp, w.causal, n)
     rng = np.random.default_rng(3)
