@@ -256,15 +256,27 @@ size_t splitkv_bytes(int64_t rows, int D, int num_splits) {
 }
 
 // Key slices for a split-KV call on a GPU of num_sms SMs, given the CTAs of
-// one slice (units): enough CTAs for about four per SM, each slice at least
-// four 128-key tiles, no empty slice.
+// one slice (units).  Each slice keeps at least four 128-key tiles.  The
+// count minimises a simple time model: the waves of CTAs (one CTA per SM at
+// a time) times the tiles of one CTA plus a fixed cost of about two tiles
+// (Q load, tensor-memory setup, partial-state write), so that the last wave
+// is not left mostly idle.  1 when the query tiles alone fill the GPU.
 int plan_splits(int64_t units, int64_t key_tiles, int num_sms) {
   if (units <= 0 || key_tiles < 8 || units >= 2 * (int64_t)num_sms) return 1;
-  int64_t splits = (4 * (int64_t)num_sms + units - 1) / units;
-  splits = std::min<int64_t>(splits, std::max<int64_t>(1, key_tiles / 4));
-  splits = std::min<int64_t>(splits, kMaxSplits);
-  const int64_t per = (key_tiles + splits - 1) / splits;
-  return (int)((key_tiles + per - 1) / per);
+  auto cost = [&](int64_t s, int64_t per) { return ((units * s + num_sms - 1) / num_sms) * (per + 2); };
+  int best = 1;
+  int64_t best_cost = cost(1, key_tiles);
+  const int64_t s_max = std::min<int64_t>(key_tiles / 4, kMaxSplits);
+  for (int64_t s = 2; s <= s_max; ++s) {
+    const int64_t per = (key_tiles + s - 1) / s;
+    if ((key_tiles + per - 1) / per != s) continue;  // the same slices as a smaller count
+    const int64_t c = cost(s, per);
+    if (c < best_cost) {
+      best = (int)s;
+      best_cost = c;
+    }
+  }
+  return best;
 }
 
 // Split-KV arguments of fwd_impl.
