@@ -13,6 +13,9 @@ Modules
 ``online_state`` the mergeable (running max m, rescaled exp-sum l, numerator
                  acc) state with its explicit empty identity, the algebra the
                  streaming method is built on.
+``backward``     the gradients dQ, dK, dV of sum(dO * O), from probabilities
+                 recomputed by the definition (dense, or sampled rows of a
+                 large problem).
 
 Sources (web pages, cited by title and section):
   * "Intermediate and advanced extension" (triton-cuda-lab), workshop table row
@@ -20,17 +23,21 @@ Sources (web pages, cited by title and section):
   * "Intermediate and advanced workshop validation" (triton-cuda-lab),
     "Correctness and review".
   * "Attention algorithms and data movement" (study.greatitself.com), lessons
-    01 (merging normalised attention), 04 (packed causal eligibility) and 05
-    (GQA head mapping).
+    01 (merging normalised attention), 03 (differentiating the normalised
+    row), 04 (packed causal eligibility, unequal lengths), 05 (GQA head
+    mapping) and 07 (local windows).
 
 Parity status: every function here is pinned by CPU tests in
-``tests/test_oracle.py`` against closed forms, a hand-worked example, library
-routines (PyTorch's CPU scaled_dot_product_attention, SciPy's logsumexp),
-invariants and brute force; none is "parity unpinned".
+``tests/test_oracle.py``, ``tests/test_oracle_lengths.py`` and
+``tests/test_oracle_backward.py`` against closed forms, a hand-worked example, library
+routines (PyTorch's CPU scaled_dot_product_attention and its float64
+autograd, SciPy's logsumexp), finite differences, invariants and brute
+force; none is "parity unpinned".
 """
 
 from .dense import attention_dense, attention_varlen, attention_rows, attention_varlen_rows
 from .online_state import State, empty_state, state_of_block, merge, finalize
+from .backward import attention_backward_dense, attention_backward_sampled
 
 __all__ = [
     "attention_dense",
@@ -42,4 +49,6 @@ __all__ = [
     "state_of_block",
     "merge",
     "finalize",
+    "attention_backward_dense",
+    "attention_backward_sampled",
 ]
