@@ -1,6 +1,7 @@
 """ctypes binding of the C ABI in ``include/etattn.h``.
 
-The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_fwd_splitkv``, ``attn_fwd_splitkv_noalloc``,
+The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_size``,
+``attn_fwd_splitkv``, ``attn_fwd_splitkv_noalloc``,
 ``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
@@ -71,6 +72,11 @@ def load_library(path: str | None = None):
         lib.attn_fwd_splitkv.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _int, _vp,
                                          ctypes.c_size_t, _vp])
         lib.attn_fwd_splitkv.restype = _int
+        lib.attn_bwd.argtypes = [_vp] * 9 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _vp, ctypes.c_size_t,
+                                                                                   _vp]
+        lib.attn_bwd.restype = _int
+        lib.attn_bwd_workspace_size.argtypes = [_int] * 4
+        lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv_noalloc.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 +
                                                  [ctypes.c_float, _int, _vp])
         lib.attn_fwd_splitkv_noalloc.restype = _int
@@ -126,6 +132,19 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, cau
     return lib.attn_fwd_splitkv(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D,
                                 dtype, _strides_arg(strides), causal, window_left, window_right, scale, num_splits,
                                 workspace or None, workspace_bytes, stream or None)
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left,
+             window_right, scale, workspace, workspace_bytes, stream):
+    """C ``attn_bwd``: pointers as ints (0 for NULL), ``strides`` 32 ints."""
+    lib = load_library()
+    return lib.attn_bwd(q or None, k or None, v or None, o or None, lse or None, dout or None, dq or None, dk or None,
+                        dv or None, B, Hq, Hkv, Nq, Nk, D, dtype, _strides_arg(strides), causal, window_left,
+                        window_right, scale, workspace or None, workspace_bytes, stream or None)
+
+
+def attn_bwd_workspace_size(B, Hq, Nq, D) -> int:
+    return load_library().attn_bwd_workspace_size(B, Hq, Nq, D)
 
 
 def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left,
@@ -303,6 +322,43 @@ def attention_splitkv(q, k, v, *, causal: bool = True, scale: float | None = Non
     if rc != 0:
         raise EtattnError(rc, "attn_fwd_splitkv")
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, *, causal: bool = True, scale: float | None = None,
+                       window_left: int = -1, window_right: int = -1, dq=None, dk=None, dv=None, workspace=None,
+                       stream=None):
+    """Gradients (dq, dk, dv) of ``attention`` for upstream gradient ``dout``,
+    given the forward's output ``o`` and logsumexp ``lse`` ([B, Hq, Nq] FP32).
+    Shapes and strides as for ``attention``; the outputs are allocated when
+    not given, and so is the FP32 workspace (``attn_bwd_workspace_size``)."""
+    import torch
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
+    with torch.cuda.device(q.device):
+        if dq is None:
+            dq = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
+        if dk is None:
+            dk = torch.empty((B, Hkv, Nk, D), dtype=q.dtype, device=q.device)
+        if dv is None:
+            dv = torch.empty((B, Hkv, Nk, D), dtype=q.dtype, device=q.device)
+        need = attn_bwd_workspace_size(B, Hq, Nq, D)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        strides = [*q.stride(), *k.stride(), *v.stride(), *o.stride(), *dout.stride(), *dq.stride(), *dk.stride(),
+                   *dv.stride()]
+        ws_ptr = workspace.data_ptr() if workspace is not None else 0
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Nq, Nk, D, _dtype_code(q), strides,
+                      1 if causal else 0, int(window_left), int(window_right), float(scale), ws_ptr, ws_bytes,
+                      _stream_handle(stream))
+    if rc != 0:
+        raise EtattnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = True, scale: float | None = None,

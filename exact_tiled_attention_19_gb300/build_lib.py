@@ -73,10 +73,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
               os.path.join(BUILD_DIR, "attn_api.o")], "attn_api"),
             ([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, "attn_combine.cu"), "-o",
               os.path.join(BUILD_DIR, "attn_combine.o")], "attn_combine")]
-    for d, bf in VARIANTS:
-        obj = os.path.join(BUILD_DIR, f"attn_fwd_d{d}_{bf}.o")
-        jobs.append(([nvcc, *ARCH, *CFLAGS, f"-DETATTN_INST_D={d}", f"-DETATTN_INST_BF16={bf}", "-c",
-                      os.path.join(CSRC, "attn_fwd_inst.cu"), "-o", obj], f"d{d}_{bf}"))
+    jobs.append(([nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, "attn_bwd_aux.cu"), "-o",
+                  os.path.join(BUILD_DIR, "attn_bwd_aux.o")], "attn_bwd_aux"))
+    for kind in ("fwd", "bwd"):
+        for d, bf in VARIANTS:
+            obj = os.path.join(BUILD_DIR, f"attn_{kind}_d{d}_{bf}.o")
+            jobs.append(([nvcc, *ARCH, *CFLAGS, f"-DETATTN_INST_D={d}", f"-DETATTN_INST_BF16={bf}", "-c",
+                          os.path.join(CSRC, f"attn_{kind}_inst.cu"), "-o", obj], f"{kind}_d{d}_{bf}"))
     with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
         logs = list(ex.map(lambda j: (j[1], _run(j[0])), jobs))
     if verbose:

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include "attn_bwd_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "etattn.h"
 #include "launchers.h"
@@ -456,6 +457,175 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ETATTN_OK;
 }
 
+// Backward workspace: FP32 dQ [B, Hq, Nq, D], then at 256-byte boundaries the
+// per-row lse * log2(e) and D = <dO, O>, each [B * Hq][Nq_pad].
+struct BwdLayout {
+  size_t dq_off, lse2_off, dvec_off, total;
+};
+BwdLayout bwd_layout(int64_t B, int64_t Hq, int64_t Nq, int D) {
+  auto up = [](size_t x) { return (x + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign; };
+  const int64_t nq_pad = (Nq + 127) / 128 * 128;
+  BwdLayout L{};
+  L.dq_off = 0;
+  L.lse2_off = up((size_t)(B * Hq * Nq) * D * 4);
+  L.dvec_off = L.lse2_off + up((size_t)(B * Hq * nq_pad) * 4);
+  L.total = L.dvec_off + up((size_t)(B * Hq * nq_pad) * 4);
+  return L;
+}
+
+// Backward pass: validation, then three launches on `stream` (row
+// statistics, the backward kernel, dQ conversion).
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype, const int64_t* strides,
+             int causal, int window_left, int window_right, float scale, void* workspace, size_t workspace_bytes,
+             void* stream) {
+  if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
+  if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
+  if (Nq > kMaxTokens || Nk > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
+  if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
+  if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
+  if (B == 0 || Hq == 0 || (Nq == 0 && Nk == 0)) return ETATTN_OK;
+  const bool has_q = Nq > 0, has_k = Nk > 0;
+  if (has_q && (!q || !o || !lse || !dout || !dq)) return ETATTN_ERR_NULL_PTR;
+  if (has_k && (!k || !v || !dk || !dv)) return ETATTN_ERR_NULL_PTR;
+  const int64_t* st = strides;
+  auto view = [&](const void* ptr, int idx, int H, int N) {
+    return View{ptr, 4, {B, H, N, D}, {st[4 * idx], st[4 * idx + 1], st[4 * idx + 2], st[4 * idx + 3]}};
+  };
+  const View vq = view(q, 0, Hq, Nq), vk = view(k, 1, Hkv, Nk), vv = view(v, 2, Hkv, Nk), vo = view(o, 3, Hq, Nq);
+  const View vdo = view(dout, 4, Hq, Nq), vdq = view(dq, 5, Hq, Nq), vdk = view(dk, 6, Hkv, Nk),
+             vdv = view(dv, 7, Hkv, Nk);
+  const View vl{lse, 3, {B, Hq, Nq, 0}, {(int64_t)Hq * Nq, Nq, 1, 0}};
+  for (const View* t : {&vq, &vk, &vv, &vo, &vdo, &vdq, &vdk, &vdv})
+    if (!strides_ok(*t, 2)) return ETATTN_ERR_BAD_STRIDE;
+  if (has_q)
+    for (const void* ptr : {q, o, dout, (const void*)dq})
+      if (!aligned16(ptr)) return ETATTN_ERR_BAD_ALIGN;
+  if (has_k)
+    for (const void* ptr : {k, v, (const void*)dk, (const void*)dv})
+      if (!aligned16(ptr)) return ETATTN_ERR_BAD_ALIGN;
+  if (has_q && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ETATTN_ERR_BAD_ALIGN;
+  // Outputs overlap no input and no other output.
+  const BwdLayout L = bwd_layout(B, Hq, Nq, D);
+  const View vw{workspace, 1, {(int64_t)L.total, 0, 0, 0}, {1, 0, 0, 0}};
+  for (const View* out : {&vdq, &vdk, &vdv}) {
+    for (const View* in : {&vq, &vk, &vv, &vo, &vdo})
+      if (overlaps(*out, 2, *in, 2)) return ETATTN_ERR_ALIAS;
+    if (has_q && overlaps(*out, 2, vl, 4)) return ETATTN_ERR_ALIAS;
+  }
+  if (overlaps(vdq, 2, vdk, 2) || overlaps(vdq, 2, vdv, 2) || overlaps(vdk, 2, vdv, 2)) return ETATTN_ERR_ALIAS;
+  // Workspace: FP32 dQ and row statistics, private to the call.
+  if (has_q) {
+    if (workspace == nullptr) return ETATTN_ERR_NULL_PTR;
+    if (reinterpret_cast<uintptr_t>(workspace) % kWorkspaceAlign) return ETATTN_ERR_BAD_ALIGN;
+    if (workspace_bytes < L.total) return ETATTN_ERR_BAD_SHAPE;
+    for (const View* t : {&vq, &vk, &vv, &vo, &vdo, &vdq, &vdk, &vdv})
+      if (overlaps(vw, 1, *t, 2)) return ETATTN_ERR_ALIAS;
+    if (overlaps(vw, 1, vl, 4)) return ETATTN_ERR_ALIAS;
+  }
+
+  int dev = 0;
+  int* status = nullptr;
+  int num_sms = 0;
+  if (int rc = current_device(&dev, &status, &num_sms)) return rc;
+  (void)num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf = dtype == ETATTN_BF16;
+  const int nq_pad = (Nq + 127) / 128 * 128;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dq_acc = has_q ? reinterpret_cast<float*>(ws + L.dq_off) : nullptr;
+  float* lse2 = has_q ? reinterpret_cast<float*>(ws + L.lse2_off) : nullptr;
+  float* dvec = has_q ? reinterpret_cast<float*>(ws + L.dvec_off) : nullptr;
+
+  if (has_q) {
+    BwdPreParams pp{};
+    pp.o = o;
+    pp.dout = dout;
+    pp.lse = lse;
+    pp.o_sb = st[12];
+    pp.o_sh = st[13];
+    pp.o_sn = st[14];
+    pp.do_sb = st[16];
+    pp.do_sh = st[17];
+    pp.do_sn = st[18];
+    pp.rows = (int64_t)B * Hq * nq_pad;
+    pp.Hq = Hq;
+    pp.Nq = Nq;
+    pp.Nq_pad = nq_pad;
+    pp.dvec = dvec;
+    pp.lse2 = lse2;
+    pp.dq_acc = dq_acc;
+    cudaError_t e = launch_bwd_pre(D, bf, pp, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  if (has_k) {
+    CUtensorMap mq, mk, mv, mdo;
+    bool swq = false, swk = false, swv = false, swd = false;
+    if (int rc = encode_map(&mk, dtype, k, D, Nk, Hkv, B, st[6], st[5], st[4], &swk)) return rc;
+    if (int rc = encode_map(&mv, dtype, v, D, Nk, Hkv, B, st[10], st[9], st[8], &swv)) return rc;
+    if (has_q) {
+      if (int rc = encode_map(&mq, dtype, q, D, Nq, Hq, B, st[2], st[1], st[0], &swq)) return rc;
+      if (int rc = encode_map(&mdo, dtype, dout, D, Nq, Hq, B, st[18], st[17], st[16], &swd)) return rc;
+    } else {
+      // No queries: every key's gradient is 0 and no Q / dO tile is loaded;
+      // the key map stands in for the unused ones.
+      mq = mk;
+      mdo = mk;
+    }
+    BwdParams p{};
+    p.dk = dk;
+    p.dv = dv;
+    p.dk_sb = st[24];
+    p.dk_sh = st[25];
+    p.dk_sn = st[26];
+    p.dv_sb = st[28];
+    p.dv_sh = st[29];
+    p.dv_sn = st[30];
+    p.dq_acc = dq_acc;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.Nq_pad = nq_pad;
+    p.Hq = Hq;
+    p.group = Hq / Hkv;
+    p.win_left = window_left_of(window_left);
+    p.win_right = window_right_of(window_right, causal);
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = status;
+    p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0) | (swd ? 8 : 0);
+    const dim3 grid((unsigned)((Nk + 127) / 128), (unsigned)Hkv, (unsigned)B);
+    cudaError_t e;
+    switch (D) {
+      case 32:
+        e = bf ? launch_bwd_d32_1(mq, mk, mv, mdo, p, grid, s) : launch_bwd_d32_0(mq, mk, mv, mdo, p, grid, s);
+        break;
+      case 64:
+        e = bf ? launch_bwd_d64_1(mq, mk, mv, mdo, p, grid, s) : launch_bwd_d64_0(mq, mk, mv, mdo, p, grid, s);
+        break;
+      default:
+        e = bf ? launch_bwd_d128_1(mq, mk, mv, mdo, p, grid, s) : launch_bwd_d128_0(mq, mk, mv, mdo, p, grid, s);
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  if (has_q) {
+    BwdConvertParams cp{};
+    cp.dq_acc = dq_acc;
+    cp.dq = dq;
+    cp.dq_sb = st[20];
+    cp.dq_sh = st[21];
+    cp.dq_sn = st[22];
+    cp.rows = (int64_t)B * Hq * Nq;
+    cp.Hq = Hq;
+    cp.Nq = Nq;
+    cudaError_t e = launch_bwd_convert(D, bf, cp, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return ETATTN_OK;
+}
+
 // Host mirror of packed offsets: 0, non-decreasing, ending at total, every
 // length <= max_len.
 bool seqlens_ok(const int32_t* cu, int num_seqs, int total, int max_len) {
@@ -627,6 +797,20 @@ int attn_fwd_splitkv_plan(int B, int Hq, int Hkv, int Nq, int Nk, int* num_split
   const int64_t units = (int64_t)B * (Hq / P) * (((int64_t)Nq * P + 127) / 128);
   *num_splits = plan_splits(units, ((int64_t)Nk + 127) / 128, num_sms);
   return ETATTN_OK;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype, const int64_t* strides,
+             int causal, int window_left, int window_right, float scale, void* workspace, size_t workspace_bytes,
+             void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left,
+                  window_right, scale, workspace, workspace_bytes, stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int D) {
+  if (B < 0 || Hq < 0 || Nq < 0 || !head_dim_ok(D)) return 0;
+  if (B == 0 || Hq == 0 || Nq == 0) return 0;
+  return bwd_layout(B, Hq, Nq, D).total;
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens,

@@ -148,10 +148,6 @@ struct TileCfg {
                 "register split over budget");
 };
 
-__device__ __forceinline__ void fence_regs32(uint32_t* r) {
-  asm volatile("" : ETATTN_RW8(r, 0), ETATTN_RW8(r, 8), ETATTN_RW8(r, 16), ETATTN_RW8(r, 24));
-}
-
 struct SmemBarriers {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3];

@@ -203,6 +203,41 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              int window_left, int window_right, float scale, int num_splits, void* stream);
 
 /*
+ * attn_bwd: gradients of the attention of attn_fwd_ex ("Attention algorithms
+ * and data movement", lesson 03: recompute the probabilities and
+ * differentiate the normalised row from the saved normalisation state).
+ * Given the forward's inputs, its output O, its logsumexp and the upstream
+ * gradient dO, it writes
+ *     dQ = scale * dS K,   dK = scale * dS^T Q,   dV = P^T dO,
+ * with P_ij = exp(scale*<q_i,k_j> - lse_i) on eligible pairs (0 elsewhere),
+ * dS = P * (dO V^T - D) and D_i = <dO_i, O_i>.  Under grouped-query attention
+ * dK and dV of a key/value head sum over the query heads that read it.
+ *
+ *   q, o, dout, dq: logical [B, Hq, Nq, D];  k, v, dk, dv: [B, Hkv, Nk, D]
+ *   lse : [B, Hq, Nq] contiguous FP32, as attn_fwd / attn_fwd_ex wrote it
+ *         (natural log of the scaled logits; -inf on rows that read no key)
+ *   strides: 32 int64 values, (b, h, n, d) for q, k, v, o, dout, dq, dk, dv
+ *         in that order; d-strides 1, the others as for attn_fwd.
+ *   causal, window_left, window_right, scale: as for the forward call.
+ *   workspace: caller-owned DEVICE scratch, 256-byte aligned, at least
+ *         attn_bwd_workspace_size(B, Hq, Nq, D) bytes (FP32 dQ plus two FP32
+ *         values per query row), private to the call until its last launch
+ *         has run on `stream`; its contents on entry do not matter.
+ * Inputs (q, k, v, o, lse, dout) are only read.  dq, dk, dv must not overlap
+ * an input, the workspace or each other (ETATTN_ERR_ALIAS).  Nq = 0 gives dk =
+ * dv = 0 (q, o, lse, dout, dq may be NULL); Nk = 0 gives dq = 0 (k, v, dk, dv
+ * may be NULL).  The call enqueues three kernels (row statistics, the
+ * gradients, dQ conversion) and returns; errors as for attn_fwd.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int D, int dtype, const int64_t* strides,
+             int causal, int window_left, int window_right, float scale, void* workspace, size_t workspace_bytes,
+             void* stream);
+
+/* Workspace bytes attn_bwd needs (0 for empty or invalid sizes). */
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int D);
+
+/*
  * attn_fwd_varlen_ex: attn_fwd_varlen with separate packed query and key
  * offsets and an optional local window.
  *

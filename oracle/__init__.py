@@ -37,7 +37,7 @@ force; none is "parity unpinned".
 
 from .dense import attention_dense, attention_varlen, attention_rows, attention_varlen_rows
 from .online_state import State, empty_state, state_of_block, merge, finalize
-from .backward import attention_backward_dense, attention_backward_sampled
+from .backward import attention_backward_dense, attention_backward_sampled, backward_magnitudes
 
 __all__ = [
     "attention_dense",
@@ -51,4 +51,5 @@ __all__ = [
     "finalize",
     "attention_backward_dense",
     "attention_backward_sampled",
+    "backward_magnitudes",
 ]

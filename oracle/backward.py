@@ -93,13 +93,14 @@ def attention_backward_dense(q, k, v, do, *, causal, scale, window_left=-1, wind
 
 
 def attention_backward_sampled(q, k, v, do, q_rows, k_rows, *, causal, scale, group=1, window_left=-1,
-                               window_right=-1):
+                               window_right=-1, magnitudes=False):
     """Selected gradient rows of one (batch, KV head) of a large problem.
 
     q, do: [G, Nq, D] for the ``group`` query heads that read the KV head;
     k, v: [Nk, D].  Returns dq [G, len(q_rows), D] and dk, dv
     [len(k_rows), D].  Every query row's probabilities are recomputed (in
-    chunks), so dK and dV hold the full sums over queries and heads."""
+    chunks), so dK and dV hold the full sums over queries and heads.  With
+    ``magnitudes`` the same rows of backward_magnitudes follow."""
     q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
     G, Nq = q.shape[0], q.shape[1]
     if G != group:
@@ -109,6 +110,7 @@ def attention_backward_sampled(q, k, v, do, q_rows, k_rows, *, causal, scale, gr
     dq = np.zeros((G, len(q_rows), q.shape[2]))
     dk = np.zeros((len(k_rows), k.shape[1]))
     dv = np.zeros((len(k_rows), v.shape[1]))
+    mq, mk, mv = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)
     for g in range(G):
         for r0 in range(0, Nq, _ROW_CHUNK):
             rows = np.arange(r0, min(Nq, r0 + _ROW_CHUNK))
@@ -121,4 +123,41 @@ def attention_backward_sampled(q, k, v, do, q_rows, k_rows, *, causal, scale, gr
             sel = np.nonzero((q_rows >= r0) & (q_rows < r0 + len(rows)))[0]
             if len(sel):
                 dq[g, sel] = scale * (ds[q_rows[sel] - r0] @ k)
+            if magnitudes:
+                adp = np.abs(dp)
+                a = p * (adp + np.sum(p * adp, axis=1)[:, None])
+                mv += p[:, k_rows].T @ np.abs(do[g, rows])
+                mk += scale * (a[:, k_rows].T @ np.abs(q[g, rows]))
+                if len(sel):
+                    mq[g, sel] = scale * (a[q_rows[sel] - r0] @ np.abs(k))
+    if magnitudes:
+        return dq, dk, dv, mq, mk, mv
     return dq, dk, dv
+
+
+def backward_magnitudes(q, k, v, do, *, causal, scale, window_left=-1, window_right=-1):
+    """Sums of the absolute values of the terms of each gradient element, the
+    scale against which rounding errors in a 16-bit implementation are
+    measured (not a result the kernel computes):
+      M_dV_j = sum_i P_ij |dO_i|
+      A_ij   = P_ij (|dP_ij| + sum_l P_il |dP_il|)
+      M_dQ_i = scale * sum_j A_ij |k_j|,   M_dK_j = scale * sum_i A_ij |q_i|
+    Shapes as in attention_backward_dense (dK, dV terms summed over the group)."""
+    q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
+    B, Hq, Nq, D = q.shape
+    group = Hq // k.shape[1]
+    mq = np.zeros_like(q)
+    mk = np.zeros_like(k)
+    mv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            hk = kv_head_of(h, group)
+            for r0 in range(0, Nq, _ROW_CHUNK):
+                rows = np.arange(r0, min(Nq, r0 + _ROW_CHUNK))
+                p = _probabilities(q[b, h, rows], rows, k[b, hk], causal, scale, Nq, window_left, window_right)
+                adp = np.abs(do[b, h, rows] @ v[b, hk].T)
+                a = p * (adp + np.sum(p * adp, axis=1)[:, None])
+                mv[b, hk] += p.T @ np.abs(do[b, h, rows])
+                mq[b, h, rows] = scale * (a @ np.abs(k[b, hk]))
+                mk[b, hk] += scale * (a.T @ np.abs(q[b, h, rows]))
+    return mq, mk, mv

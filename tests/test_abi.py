@@ -302,3 +302,42 @@ def test_noalloc_refuses_problems_beyond_its_scratch_before_any_device_work():
     assert noalloc_call(num_splits=0) == 3
     assert noalloc_call(num_splits=4, o=Q + 64) == 7
     assert noalloc_call(num_splits=4, N=0) == 0
+
+
+DQ, DK, DV, DO, OO, WS = 0x80000000, 0x90000000, 0xA0000000, 0xB0000000, 0xC0000000, 0xD0000000
+
+
+def bwd_call(**kw):
+    a = dict(q=Q, k=K, v=V, o=OO, lse=LSE, dout=DO, dq=DQ, dk=DK, dv=DV, B=2, Hq=4, Hkv=2, Nq=100, Nk=120, D=64,
+             dtype=1, causal=1, wl=-1, wr=-1, scale=0.125, ws=WS, ws_bytes=1 << 26, stream=0)
+    a.update(kw)
+    qs = contiguous_strides(a["B"], a["Hq"], a["Nq"], a["D"])
+    ks = contiguous_strides(a["B"], a["Hkv"], a["Nk"], a["D"])
+    st = qs + ks + ks + qs + qs + qs + ks + ks
+    return B.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"], a["dv"], a["B"], a["Hq"],
+                      a["Hkv"], a["Nq"], a["Nk"], a["D"], a["dtype"], st, a["causal"], a["wl"], a["wr"], a["scale"],
+                      a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=5), 2), (dict(D=48), 3), (dict(Nk=-1), 3), (dict(Hkv=3), 4), (dict(scale=0.0), 8),
+    (dict(lse=0), 1), (dict(dout=0), 1), (dict(dk=0), 1), (dict(ws=0), 1),
+    (dict(dq=DQ + 8), 6), (dict(ws=WS + 16), 6), (dict(ws_bytes=1000), 3),
+    (dict(dq=Q + 128), 7), (dict(dk=DV), 7), (dict(ws=DQ), 7), (dict(dv=LSE), 7),
+])
+def test_bwd_invalid_arguments_rejected(kw, code):
+    assert bwd_call(**kw) == code
+
+
+def test_bwd_workspace_and_empty_calls():
+    import torch
+    rows = 2 * 4 * 100
+    n_pad = 2 * 4 * 128
+    up = lambda x: (x + 255) // 256 * 256
+    assert B.attn_bwd_workspace_size(2, 4, 100, 64) == up(rows * 64 * 4) + 2 * up(n_pad * 4)
+    assert B.attn_bwd_workspace_size(2, 4, 0, 64) == 0
+    assert bwd_call(B=0) == 0
+    assert bwd_call(Nq=0, Nk=0) == 0
+    want = 12 if not torch.cuda.is_available() else 0
+    assert bwd_call() == want
+    assert bwd_call(Nq=0, q=0, o=0, lse=0, dout=0, dq=0, ws=0, ws_bytes=0) == want  # no queries: dk = dv = 0

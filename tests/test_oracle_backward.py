@@ -127,6 +127,13 @@ def test_sampled_rows_equal_dense(causal, wl):
                                                          scale=0.3, group=2, window_left=wl)
         assert np.max(np.abs(sq - dq[0, 2 * hk:2 * hk + 2][:, qr])) < 1e-12
         assert np.max(np.abs(sk - dk[0, hk, kr])) < 1e-12 and np.max(np.abs(sv - dv[0, hk, kr])) < 1e-12
+    mq, mk, mv = backward.backward_magnitudes(q, k, v, do, causal=causal, scale=0.3, window_left=wl)
+    for hk in range(2):
+        out = backward.attention_backward_sampled(q[0, 2 * hk:2 * hk + 2], k[0, hk], v[0, hk], do[0, 2 * hk:2 * hk + 2],
+                                                  qr, kr, causal=causal, scale=0.3, group=2, window_left=wl,
+                                                  magnitudes=True)
+        assert np.max(np.abs(out[3] - mq[0, 2 * hk:2 * hk + 2][:, qr])) < 1e-12
+        assert np.max(np.abs(out[4] - mk[0, hk, kr])) < 1e-12 and np.max(np.abs(out[5] - mv[0, hk, kr])) < 1e-12
 
 
 # ---------------------------------------------------------------- planted mistakes
@@ -181,3 +188,20 @@ def test_mutation_group_overwrite_is_caught(monkeypatch):
         return dq, last[1], last[2]
     monkeypatch.setattr(backward, "attention_backward_dense", bad)
     assert _torch_error() > 1e-3
+
+
+def test_magnitudes_bound_the_gradients():
+    """Each magnitude is a sum of absolute values of the terms its gradient
+    element sums, so it bounds the element (triangle inequality); with
+    dO >= 0 the value-gradient terms are nonnegative and M_dV equals dV."""
+    q, do = rnd((1, 4, 30, 8), 29), rnd((1, 4, 30, 8), 30)
+    k, v = rnd((1, 2, 40, 8), 31), rnd((1, 2, 40, 8), 32)
+    for kw in (dict(causal=True), dict(causal=False, window_left=5, window_right=2)):
+        g = backward.attention_backward_dense(q, k, v, do, scale=0.3, **kw)
+        m = backward.backward_magnitudes(q, k, v, do, scale=0.3, **kw)
+        for gi, mi in zip(g, m):
+            assert np.all(mi >= np.abs(gi) - 1e-12)
+    dop = np.abs(do)
+    _, _, dv = backward.attention_backward_dense(q, k, v, dop, causal=True, scale=0.3)
+    _, _, mv = backward.backward_magnitudes(q, k, v, dop, causal=True, scale=0.3)
+    assert np.max(np.abs(mv - dv)) < 1e-12
