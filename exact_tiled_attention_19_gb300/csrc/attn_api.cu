@@ -227,6 +227,23 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
 
 bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 128; }
 
+// 3-D FP32 map over the backward's dQ buffer [rows_bh = B * Hq][Nq][D] for
+// TMA reduce-adds of (32 columns x 128 rows) boxes, 128-byte swizzled; rows
+// past Nq of a (batch, head) fall outside the map.
+int encode_dq_map(CUtensorMap* map, float* dq_acc, int D, int64_t Nq, int64_t rows_bh) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return fail_cuda(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Nq, (cuuint64_t)rows_bh};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)Nq * D * 4};
+  cuuint32_t box[3] = {32u, 128u, 1u};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+  return ETATTN_OK;
+}
+
 constexpr int kMaxSplits = 1024;
 
 // Query heads packed into one 128-row tile: the largest power of two that
@@ -458,7 +475,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 }
 
 // Backward workspace: FP32 dQ [B, Hq, Nq, D], then at 256-byte boundaries the
-// per-row lse * log2(e) and D = <dO, O>, each [B * Hq][Nq_pad].
+// per-row -lse * log2(e) and -scale * <dO, O>, each [B * Hq][Nq_pad].
 struct BwdLayout {
   size_t dq_off, lse2_off, dvec_off, total;
 };
@@ -535,8 +552,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   const int nq_pad = (Nq + 127) / 128 * 128;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* dq_acc = has_q ? reinterpret_cast<float*>(ws + L.dq_off) : nullptr;
-  float* lse2 = has_q ? reinterpret_cast<float*>(ws + L.lse2_off) : nullptr;
-  float* dvec = has_q ? reinterpret_cast<float*>(ws + L.dvec_off) : nullptr;
+  float* nlse2 = has_q ? reinterpret_cast<float*>(ws + L.lse2_off) : nullptr;
+  float* nsd = has_q ? reinterpret_cast<float*>(ws + L.dvec_off) : nullptr;
 
   if (has_q) {
     BwdPreParams pp{};
@@ -553,25 +570,28 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     pp.Hq = Hq;
     pp.Nq = Nq;
     pp.Nq_pad = nq_pad;
-    pp.dvec = dvec;
-    pp.lse2 = lse2;
+    pp.scale = scale;
+    pp.nsd = nsd;
+    pp.nlse2 = nlse2;
     pp.dq_acc = dq_acc;
     cudaError_t e = launch_bwd_pre(D, bf, pp, s);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   if (has_k) {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     bool swq = false, swk = false, swv = false, swd = false;
     if (int rc = encode_map(&mk, dtype, k, D, Nk, Hkv, B, st[6], st[5], st[4], &swk)) return rc;
     if (int rc = encode_map(&mv, dtype, v, D, Nk, Hkv, B, st[10], st[9], st[8], &swv)) return rc;
     if (has_q) {
       if (int rc = encode_map(&mq, dtype, q, D, Nq, Hq, B, st[2], st[1], st[0], &swq)) return rc;
       if (int rc = encode_map(&mdo, dtype, dout, D, Nq, Hq, B, st[18], st[17], st[16], &swd)) return rc;
+      if (int rc = encode_dq_map(&mdq, dq_acc, D, Nq, (int64_t)B * Hq)) return rc;
     } else {
-      // No queries: every key's gradient is 0 and no Q / dO tile is loaded;
-      // the key map stands in for the unused ones.
+      // No queries: every key's gradient is 0 and no Q / dO tile is loaded
+      // or dQ box added; the key map stands in for the unused ones.
       mq = mk;
       mdo = mk;
+      mdq = mk;
     }
     BwdParams p{};
     p.dk = dk;
@@ -582,9 +602,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     p.dv_sb = st[28];
     p.dv_sh = st[29];
     p.dv_sn = st[30];
-    p.dq_acc = dq_acc;
-    p.lse2 = lse2;
-    p.dvec = dvec;
+    p.nlse2 = nlse2;
+    p.nsd = nsd;
     p.Nq = Nq;
     p.Nk = Nk;
     p.Nq_pad = nq_pad;
@@ -600,13 +619,16 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     cudaError_t e;
     switch (D) {
       case 32:
-        e = bf ? launch_bwd_d32_1(mq, mk, mv, mdo, p, grid, s) : launch_bwd_d32_0(mq, mk, mv, mdo, p, grid, s);
+        e = bf ? launch_bwd_d32_1(mq, mk, mv, mdo, mdq, p, grid, s)
+               : launch_bwd_d32_0(mq, mk, mv, mdo, mdq, p, grid, s);
         break;
       case 64:
-        e = bf ? launch_bwd_d64_1(mq, mk, mv, mdo, p, grid, s) : launch_bwd_d64_0(mq, mk, mv, mdo, p, grid, s);
+        e = bf ? launch_bwd_d64_1(mq, mk, mv, mdo, mdq, p, grid, s)
+               : launch_bwd_d64_0(mq, mk, mv, mdo, mdq, p, grid, s);
         break;
       default:
-        e = bf ? launch_bwd_d128_1(mq, mk, mv, mdo, p, grid, s) : launch_bwd_d128_0(mq, mk, mv, mdo, p, grid, s);
+        e = bf ? launch_bwd_d128_1(mq, mk, mv, mdo, mdq, p, grid, s)
+               : launch_bwd_d128_0(mq, mk, mv, mdo, mdq, p, grid, s);
     }
     if (e != cudaSuccess) return fail_cuda(e);
   }

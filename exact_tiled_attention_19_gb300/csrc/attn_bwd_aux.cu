@@ -1,11 +1,12 @@
 // The launches before and after the attention backward kernel.
 //
 // Before ("Attention algorithms and data movement", lesson 03: the saved
-// normalisation state): for every query row, D = <dO, O> in FP32, the saved
-// logsumexp in base 2 (lse * log2(e); +inf for a row that read no key, so
-// that its recomputed probabilities are 0), and a zeroed FP32 dQ row.  Rows
-// past Nq up to the next multiple of 128 get D = 0 and +inf, so the backward
-// kernel can copy 128 values per query block without a bounds check.
+// normalisation state): for every query row, -scale * D with D = <dO, O> in
+// FP32, the negated saved logsumexp in base 2 (-lse * log2(e); -inf for a row
+// that read no key, so that its recomputed probabilities are 0), and a zeroed
+// FP32 dQ row.  Rows past Nq up to the next multiple of 128 get 0 and -inf,
+// so the backward kernel can copy 128 values per query block without a
+// bounds check.
 //
 // After: dQ, accumulated in FP32 by the backward kernel, in the input type.
 #include <cstdint>
@@ -32,7 +33,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPreParams c) {
   const int lane = threadIdx.x & 31;
   const int64_t bh = row / c.Nq_pad;
   const int q = (int)(row - bh * c.Nq_pad);
-  float d = 0.f, l2 = INFINITY;
+  float d = 0.f, l2 = -INFINITY;
   if (q < c.Nq) {
     const int64_t b = bh / c.Hq, h = bh - b * c.Hq;
     const uint16_t* o = static_cast<const uint16_t*>(c.o) + b * c.o_sb + h * c.o_sh + (int64_t)q * c.o_sn + lane * PER;
@@ -43,16 +44,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(BwdPreParams c) {
     for (int i = 0; i < PER; ++i) acc = fmaf(to_f32<BF16>(o[i]), to_f32<BF16>(g[i]), acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    d = acc;
+    d = -c.scale * acc;
     const float lse = c.lse[bh * c.Nq + q];
-    l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+    l2 = lse == -INFINITY ? -INFINITY : -lse * 1.4426950408889634f;
     float* dq = c.dq_acc + (bh * c.Nq + q) * D + lane * PER;
 #pragma unroll
     for (int i = 0; i < PER; ++i) dq[i] = 0.f;
   }
   if (lane == 0) {
-    c.dvec[row] = d;
-    c.lse2[row] = l2;
+    c.nsd[row] = d;
+    c.nlse2[row] = l2;
   }
 }
 

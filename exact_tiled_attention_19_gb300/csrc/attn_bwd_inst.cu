@@ -21,7 +21,8 @@
 namespace etattn {
 
 cudaError_t ETATTN_BWD_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const CUtensorMap& dout, const BwdParams& p, dim3 grid, cudaStream_t stream) {
+                                const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdParams& p, dim3 grid,
+                                cudaStream_t stream) {
   using C = BwdCfg<ETATTN_INST_D>;
   auto kern = attn_bwd_kernel<ETATTN_INST_D, ETATTN_INST_BF16 != 0>;
   // The dynamic shared-memory opt-in is per device; set it once per device.
@@ -31,11 +32,17 @@ cudaError_t ETATTN_BWD_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, cons
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
+    // The kernel re-splits its registers between warpgroups (setmaxnreg);
+    // the split is only valid if every thread launches with LAUNCH_REGS.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, dout, p);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, dout, dq_acc, p);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,7 @@
 // head of the group and every query block of 128 rows that can read one of
 // its keys.  dK and dV accumulate in tensor memory for the whole walk and are
 // written once; each step's dQ contribution is added to an FP32 buffer with
-// atomics (a later launch converts it to the input type).
+// TMA reduce-adds (a later launch converts it to the input type).
 //
 // The scores are formed transposed (keys as rows), so that one thread owns
 // one key for P and dS and the dK / dV products take P^T and dS^T straight
@@ -25,18 +25,23 @@
 //   dK   += dS^T Q     (A = dS^T in tensor memory, B = Q MN-major)
 //   dQ_i  = dS K       (A = dS in shared memory, MN-major; B = K MN-major)
 //
-// Roles (384 threads):
-//   warps 0-3   thread t owns key row t: P^T from S^T, dS^T from dP^T (into
-//               tensor memory and, transposed, into shared memory for dQ);
-//               the dK / dV epilogue.
-//   warps 4-7   thread t owns query row t of dQ_i: reads it from tensor memory
-//               and adds it to the FP32 dQ buffer.
-//   warp 8      TMA: K and V once; per step Q (two stages) with its lse and
-//               dO (one stage) with its D (two stages).
-//   warp 9      tensor-memory allocation and MMA issue (one thread).
+// Roles (512 threads, 4 warpgroups):
+//   warpgroups 0, 1  thread t owns key row t; warpgroup c takes the query
+//                    columns [64c, 64c + 64) of each step: P^T from S^T, then
+//                    dS^T from dP^T (into tensor memory and, transposed, into
+//                    shared memory for dQ).  Epilogue: dK (0) and dV (1).
+//   warpgroup 2      thread t owns query row t of dQ_i: reads it from tensor
+//                    memory, stages it in shared memory 32 columns at a time,
+//                    and one thread adds each staged box to the FP32 buffer.
+//   warp 12          TMA: K and V once; per step Q with its lse and dO with
+//                    its D, two stages each.  At D = 128 the dS tile of a step
+//                    takes the place of its dO tile once dV has read it.
+//   warp 13          tensor-memory allocation and MMA issue (one thread).
 //
-// Tensor memory (512 columns): dK [0, D), dV [128, 128 + D), S^T / P^T / dQ
-// [256, 384), dP^T / dS^T [384, 512).
+// Tensor memory (512 columns): dK [0, D), dV [128, 128 + D), S^T [256, 384)
+// (P^T of query columns [64c, 64c + 64) packed into [256 + 64c, 256 + 64c +
+// 32); dQ_i over [256, 256 + D) once dV has read P^T), dP^T [384, 512) (dS^T
+// packed likewise at 384 + 64c).
 #pragma once
 
 #include <cstdint>
@@ -52,9 +57,8 @@ struct BwdParams {
   void* dv;
   int64_t dk_sb, dk_sh, dk_sn;   // element strides of dk (batch, head, token); d-stride 1
   int64_t dv_sb, dv_sh, dv_sn;
-  float* dq_acc;                 // FP32 [B, Hq, Nq, D], zeroed before the launch
-  const float* lse2;             // [B * Hq][Nq_pad]: lse * log2(e); +inf where a row reads no key
-  const float* dvec;             // [B * Hq][Nq_pad]: D = <dO, O>; 0 on padding rows
+  const float* nlse2;            // [B * Hq][Nq_pad]: -lse * log2(e); -inf where a row reads no key
+  const float* nsd;              // [B * Hq][Nq_pad]: -scale * <dO, O>; 0 on padding rows
   int Nq, Nk, Nq_pad;            // Nq_pad: Nq rounded up to 128
   int Hq, group;
   int win_left, win_right;       // as in the forward pass (causal: win_right = 0)
@@ -76,29 +80,43 @@ struct BwdCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;               // two stages
-  static constexpr int OFF_DO = 4 * TILE;              // one stage
-  static constexpr int OFF_DS = 5 * TILE;              // dS, 128 queries x 128 keys, MN-major, 128B swizzle
-  static constexpr int DS_BYTES = 128 * 128 * 2;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;    // two stages of 128 floats
-  // D of a step is read until the dS of the step is written, after the dO
-  // stage has been released: two stages, by step parity.
-  static constexpr int OFF_DVEC = OFF_LSE + 2 * 512;
-  static constexpr int SMEM_BYTES = OFF_DVEC + 2 * 512 + 1024;
+  static constexpr int OFF_DO = 4 * TILE;              // two stages
+  static constexpr int DS_BYTES = 128 * 128 * 2;       // dS, 128 queries x 128 keys, MN-major, 128B swizzle
+  static constexpr bool DS_IN_DO = TILE == DS_BYTES;   // D = 128: dS of a step over its dO stage
+  static constexpr int OFF_DS = 6 * TILE;              // otherwise a tile of its own
+  static constexpr int OFF_STAGE = OFF_DS + (DS_IN_DO ? 0 : DS_BYTES);  // dQ staging: 128 rows x 32 FP32
+  static constexpr int STAGE_BYTES = 128 * 128;
+  static constexpr int OFF_LSE = OFF_STAGE + STAGE_BYTES;  // two stages of 128 floats
+  static constexpr int OFF_NSD = OFF_LSE + 2 * 512;        // two stages of 128 floats
+  static constexpr int SMEM_BYTES = OFF_NSD + 2 * 512 + 1024;
   static constexpr uint32_t SBO = 8 * SW_BYTES;
   static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384, TMEM_COLS = 512;
-  static constexpr int THREADS = 384;
-  static constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
+  static constexpr int THREADS = 512;
+  static constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
+  // Register split: 512 threads launch with 128 registers each; the dQ
+  // warpgroup (which holds a whole dQ row) grows to 168 and the TMA / MMA
+  // warpgroup shrinks to 88.  128 + 128 + 168 + 88 = 4 * 128.
+  static constexpr int LAUNCH_REGS = 128, DQ_REGS = 168, CTRL_REGS = 88;
+  static_assert(2 * LAUNCH_REGS + DQ_REGS + CTRL_REGS == 4 * LAUNCH_REGS, "register split must add up");
+  // Shared-memory offset of the dS tile of a step whose stages are `slot`.
+  static constexpr int ds_offset(int slot) { return DS_IN_DO ? OFF_DO + slot * TILE : OFF_DS; }
+  // Tensor-memory column of the packed P^T / dS^T of query columns
+  // [16 kk, 16 kk + 16): half c = kk / 4 lives at 64 c.
+  static constexpr uint32_t packed_col(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
 };
 
 struct BwdBarriers {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
-  uint64_t do_full, do_empty;
-  uint64_t s_full, dp_full;      // S^T / dP^T of the step are in tensor memory
-  uint64_t p_ready, ds_ready;    // P^T / dS^T (and dS in shared memory) written (128 arrivals)
-  uint64_t dq_full;              // dQ_i in tensor memory (the step's dK and dQ products are done)
-  uint64_t dq_empty;             // dQ_i read out (128 arrivals)
-  uint64_t kv_done;              // last dK / dV product done
+  uint64_t do_full[2], do_empty[2];  // do_empty: the stage's dO and dS are read (after dQ_i)
+  uint64_t dv_done;                  // dV_i is done (dO_i read by the tensor core for the last time)
+  uint64_t s_full, dp_full;          // S^T / dP^T of the step are in tensor memory
+  uint64_t p_ready, ds_ready;        // P^T / dS^T (and dS in shared memory) written (256 arrivals)
+  uint64_t dq_full;                  // dQ_i in tensor memory (the step's dK and dQ products are done)
+  uint64_t dq_empty;                 // dQ_i read out (128 arrivals)
+  uint64_t kv_done;                  // last dK / dV product done
+  uint64_t stage_free;               // the dQ staging box may be written (leader, once per box)
+  uint64_t stage_full;               // the dQ staging box is written (128 arrivals per box)
   uint32_t tmem_base;
 };
 
@@ -140,13 +158,14 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tmQ, const CUten
     for (int c = 0; c < C::NCHUNK; ++c)
       tma_tile(smem + C::OFF_Q + slot * C::TILE + c * 128 * C::SW_BYTES, tmQ, &sb.q_full[slot], c * C::SW_ELEMS, q0,
                h, u.b, swq);
-    bulk_load(smem + C::OFF_LSE + slot * 512, p.lse2 + vec_row, 512, &sb.q_full[slot]);
-    if (i >= 1 && !mbar_wait(&sb.do_empty, (i - 1) & 1, p.status)) return;
-    mbar_arrive_expect_tx(&sb.do_full, C::TILE + 512);
+    bulk_load(smem + C::OFF_LSE + slot * 512, p.nlse2 + vec_row, 512, &sb.q_full[slot]);
+    if (i >= 2 && !mbar_wait(&sb.do_empty[slot], ((i >> 1) - 1) & 1, p.status)) return;
+    mbar_arrive_expect_tx(&sb.do_full[slot], C::TILE + 512);
 #pragma unroll
     for (int c = 0; c < C::NCHUNK; ++c)
-      tma_tile(smem + C::OFF_DO + c * 128 * C::SW_BYTES, tmDO, &sb.do_full, c * C::SW_ELEMS, q0, h, u.b, swd);
-    bulk_load(smem + C::OFF_DVEC + slot * 512, p.dvec + vec_row, 512, &sb.do_full);
+      tma_tile(smem + C::OFF_DO + slot * C::TILE + c * 128 * C::SW_BYTES, tmDO, &sb.do_full[slot], c * C::SW_ELEMS,
+               q0, h, u.b, swd);
+    bulk_load(smem + C::OFF_NSD + slot * 512, p.nsd + vec_row, 512, &sb.do_full[slot]);
   }
 }
 
@@ -165,7 +184,8 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
   const uint64_t k_mn = smem_desc(smem_u32(smem + C::OFF_K), 128 * C::SW_BYTES, C::SBO, C::SWIZZLE);
   const uint64_t q_mn = smem_desc(smem_u32(smem + C::OFF_Q), 128 * C::SW_BYTES, C::SBO, C::SWIZZLE);
   const uint64_t do_mn = smem_desc(smem_u32(smem + C::OFF_DO), 128 * C::SW_BYTES, C::SBO, C::SWIZZLE);
-  const uint64_t ds_mn = smem_desc(smem_u32(smem + C::OFF_DS), 128 * 128, 1024, kSw128);
+  const uint64_t ds_mn0 = smem_desc(smem_u32(smem + C::ds_offset(0)), 128 * 128, 1024, kSw128);
+  const uint64_t ds_mn1 = smem_desc(smem_u32(smem + C::ds_offset(1)), 128 * 128, 1024, kSw128);
   const uint64_t slot_step = (uint64_t)(C::TILE >> 4);
   const uint32_t tDK = tmem + C::TM_DK, tDV = tmem + C::TM_DV, tS = tmem + C::TM_S, tDP = tmem + C::TM_DP;
 
@@ -173,50 +193,57 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
   for (int i = 0; i < u.steps; ++i) {
     const int slot = i & 1;
     const uint64_t q_k = q_kmaj + slot * slot_step, q_m = q_mn + slot * slot_step;
+    const uint64_t do_k = do_kmaj + slot * slot_step, do_m = do_mn + slot * slot_step;
+    const uint64_t ds_mn = slot ? ds_mn1 : ds_mn0;
     if (!mbar_wait(&sb.q_full[slot], (i >> 1) & 1, status)) return;
     if (i > 0 && !mbar_wait(&sb.dq_empty, (i - 1) & 1, status)) return;
     tc_fence_after();
     // S^T = K Q^T over d in 16-element steps.
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint64_t off = (uint64_t)(((kk / C::KSTEPS_PER_CHUNK) * 128 * C::SW_BYTES + (kk % C::KSTEPS_PER_CHUNK) * 32) >> 4);
+      const uint64_t off =
+          (uint64_t)(((kk / C::KSTEPS_PER_CHUNK) * 128 * C::SW_BYTES + (kk % C::KSTEPS_PER_CHUNK) * 32) >> 4);
       mma_ss(tS, k_kmaj + off, q_k + off, id_s, kk > 0 ? 1u : 0u);
     }
     mma_commit(&sb.s_full);
-    if (!mbar_wait(&sb.do_full, i & 1, status)) return;
+    if (!mbar_wait(&sb.do_full[slot], (i >> 1) & 1, status)) return;
     tc_fence_after();
     // dP^T = V dO^T.
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint64_t off = (uint64_t)(((kk / C::KSTEPS_PER_CHUNK) * 128 * C::SW_BYTES + (kk % C::KSTEPS_PER_CHUNK) * 32) >> 4);
-      mma_ss(tDP, v_kmaj + off, do_kmaj + off, id_s, kk > 0 ? 1u : 0u);
+      const uint64_t off =
+          (uint64_t)(((kk / C::KSTEPS_PER_CHUNK) * 128 * C::SW_BYTES + (kk % C::KSTEPS_PER_CHUNK) * 32) >> 4);
+      mma_ss(tDP, v_kmaj + off, do_k + off, id_s, kk > 0 ? 1u : 0u);
     }
     mma_commit(&sb.dp_full);
-    // dV += P^T dO over the step's 128 queries, 16 at a time (8 packed columns).
+    // dV += P^T dO over the step's 128 queries, 16 at a time.
     if (!mbar_wait(&sb.p_ready, i & 1, status)) return;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ts(tDV, tS + kk * 8, do_mn + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-    mma_commit(&sb.do_empty);
+      mma_ts(tDV, tS + C::packed_col(kk), do_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv,
+             (i > 0 || kk > 0) ? 1u : 0u);
+    mma_commit(&sb.dv_done);
     // dK += dS^T Q, then dQ_i = dS K (over the 128 keys) into the S^T columns.
     if (!mbar_wait(&sb.ds_ready, i & 1, status)) return;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ts(tDK, tDP + kk * 8, q_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+      mma_ts(tDK, tDP + C::packed_col(kk), q_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv,
+             (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ss(tS, ds_mn + (uint64_t)((kk * 16 * 128) >> 4), k_mn + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_q,
              kk > 0 ? 1u : 0u);
     mma_commit(&sb.dq_full);
     mma_commit(&sb.q_empty[slot]);
+    mma_commit(&sb.do_empty[slot]);
   }
   mma_commit(&sb.kv_done);
   // Drain the arrivals no other role consumes.
   for (int i = u.steps > 2 ? u.steps - 2 : 0; i < u.steps; ++i)
-    if (!mbar_wait(&sb.q_empty[i & 1], (i >> 1) & 1, status)) return;
-  if (u.steps > 0 && !mbar_wait(&sb.do_empty, (u.steps - 1) & 1, status)) return;
+    if (!mbar_wait(&sb.q_empty[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.do_empty[i & 1], (i >> 1) & 1, status))
+      return;
 }
 
 __device__ __forceinline__ bool bwd_warp_wait(uint64_t* bar, uint32_t parity, int* status) {
@@ -229,24 +256,29 @@ template <bool BF16>
 __device__ __forceinline__ uint32_t bwd_pack(float lo, float hi) {
   return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
+// The two 16-bit values of a packed word as floats (low half first).
 template <bool BF16>
-__device__ __forceinline__ float bwd_lo(uint32_t w) {
-  return BF16 ? __uint_as_float(w << 16) : __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
-}
-template <bool BF16>
-__device__ __forceinline__ float bwd_hi(uint32_t w) {
-  return BF16 ? __uint_as_float(w & 0xffff0000u) : __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+__device__ __forceinline__ void bwd_unpack(uint32_t w, float& lo, float& hi) {
+  if (BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = f.x;
+    hi = f.y;
+  }
 }
 
-// Warps 0-3: thread t owns key kb0 + t.
+// Warpgroups 0 and 1: thread t owns key kb0 + t; warpgroup `half` the query
+// columns [64 half, 64 half + 64) of every step.
 template <int D, bool BF16>
 __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint32_t tmem, const BwdUnit u,
-                                            const BwdParams& p) {
+                                            const BwdParams& p, int half) {
   using C = BwdCfg<D>;
   constexpr uint32_t FULL = 0xffffffffu;
   const int t = threadIdx.x & 127;
-  const uint32_t lane_off = (uint32_t)((threadIdx.x >> 5) * 32) << 16;
-  const uint32_t tS = tmem + C::TM_S + lane_off, tDP = tmem + C::TM_DP + lane_off;
+  const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = tmem + C::TM_S + lane_off + 64 * half, tDP = tmem + C::TM_DP + lane_off + 64 * half;
   const int key = u.kb0 + t;
   // Query rows that may read this key: c - win_left <= key <= c + win_right
   // with c = q + Nk - Nq, i.e. q in [key - delta - win_right, key - delta + win_left].
@@ -255,76 +287,82 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
   if (qhi > p.Nq - 1) qhi = p.Nq - 1;
   if (qlo < 0) qlo = 0;
   if (key >= p.Nk) qhi = -1;  // padding key: no query reads it
-  const float c2 = p.scale_log2;
-  const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LSE);
-  const float* dvec_s = reinterpret_cast<const float*>(smem + C::OFF_DVEC);
-  uint8_t* ds_row = smem + C::OFF_DS + t * 128;
+  const float c2 = p.scale_log2, scale = p.scale;
   int* status = p.status;
 
   for (int i = 0; i < u.steps; ++i) {
-    const int q0 = u.q0(i), slot = i & 1;
+    const int q0 = u.q0(i) + 64 * half, slot = i & 1;
     const int64_t lo_rel = qlo - q0, hi_rel = qhi - q0;
-    const int lim_lo = lo_rel < -1 ? -1 : (int)lo_rel, lim_hi = hi_rel > 128 ? 128 : (int)hi_rel;
-    const bool warp_masked = __any_sync(FULL, lim_lo > 0 || lim_hi < 127);
-    const float* lse = lse_s + slot * 128;
-    const float* dvec = dvec_s + slot * 128;
-    // ---- P^T = exp2(c2 * s - lse2): two 64-column halves, written over S^T.
+    const int lim_lo = lo_rel < -1 ? -1 : (int)lo_rel, lim_hi = hi_rel > 64 ? 64 : (int)hi_rel;
+    const bool warp_masked = __any_sync(FULL, lim_lo > 0 || lim_hi < 63);
+    const float2* nlse = reinterpret_cast<const float2*>(smem + C::OFF_LSE + slot * 512) + 32 * half;
+    const float2* nsd = reinterpret_cast<const float2*>(smem + C::OFF_NSD + slot * 512) + 32 * half;
+    // ---- P^T = exp2(c2 * s - lse2), 32 columns at a time, packed over the
+    // first of this half's S^T columns.
     if (!bwd_warp_wait(&sb.s_full, i & 1, status)) return;
     tc_fence_after();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t sr[64];
-      tmem_ld_x32(tS + half * 64, sr);
-      tmem_ld_x32(tS + half * 64 + 32, sr + 32);
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t sr[32];
+      tmem_ld_x32(tS + 32 * ch, sr);
       tmem_ld_wait32(sr);
-      fence_regs32(sr + 32);
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const int c = half * 64 + j;
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), c2, -lse[c]));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), c2, -lse[c + 1]));
+      for (int j = 0; j < 32; j += 2) {
+        const int c = 32 * ch + j;
+        const float2 nl = nlse[c / 2];
+        float p0, p1;
+        fma2(p0, p1, __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]), c2, c2, nl.x, nl.y);
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
         if (warp_masked) {
           p0 = (c < lim_lo || c > lim_hi) ? 0.f : p0;
           p1 = (c + 1 < lim_lo || c + 1 > lim_hi) ? 0.f : p1;
         }
         pk[j / 2] = bwd_pack<BF16>(p0, p1);
       }
-      tmem_st_x32(tS + half * 32, pk);
+      tmem_st_x16(tS + 16 * ch, pk);
     }
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&sb.p_ready);
 
-    // ---- dS^T = scale * P (dP - D), over dP^T in tensor memory and, as dS,
-    // into shared memory (row t = key t; 16-byte unit u of queries 8u..8u+7
-    // of each 64-query half at unit u ^ (t mod 8): the 128-byte swizzle).
+    // ---- dS^T = P (scale * dP - scale * D), over this half's dP^T columns
+    // and, as dS, into shared memory: row t = key t, 16-byte unit u of
+    // queries 8u .. 8u + 7 of the half at unit u ^ (t mod 8) (128B swizzle).
     if (!bwd_warp_wait(&sb.dp_full, i & 1, status)) return;
-    if (i > 0 && !bwd_warp_wait(&sb.dq_full, (i - 1) & 1, status)) return;  // dQ_{i-1} has read dS
     tc_fence_after();
+    uint8_t* ds_row = smem + C::ds_offset(slot) + half * (128 * 128) + t * 128;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t dr[64], pk[32];
-      tmem_ld_x32(tDP + half * 64, dr);
-      tmem_ld_x32(tDP + half * 64 + 32, dr + 32);
-      tmem_ld_x32(tS + half * 32, pk);
-      tmem_ld_wait32(dr);
-      fence_regs32(dr + 32);
-      fence_regs32(pk);
-      uint32_t ds[32];
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t dr[32], pk[16];
+      tmem_ld_x32(tDP + 32 * ch, dr);
+      tmem_ld_x16(tS + 16 * ch, pk);
+      tmem_ld_wait32(dr);  // waits for both loads
+      fence_regs16(pk);
+      uint32_t ds[16];
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const int c = half * 64 + j;
-        const float d0 = bwd_lo<BF16>(pk[j / 2]) * (__uint_as_float(dr[j]) - dvec[c]) * p.scale;
-        const float d1 = bwd_hi<BF16>(pk[j / 2]) * (__uint_as_float(dr[j + 1]) - dvec[c + 1]) * p.scale;
-        ds[j / 2] = bwd_pack<BF16>(d0, d1);
+      for (int j = 0; j < 32; j += 2) {
+        const float2 nd = nsd[(32 * ch + j) / 2];
+        float p0, p1, g0, g1;
+        bwd_unpack<BF16>(pk[j / 2], p0, p1);
+        fma2(g0, g1, __uint_as_float(dr[j]), __uint_as_float(dr[j + 1]), scale, scale, nd.x, nd.y);
+        fma2(g0, g1, p0, p1, g0, g1, 0.f, 0.f);
+        ds[j / 2] = bwd_pack<BF16>(g0, g1);
       }
-      tmem_st_x32(tDP + half * 32, ds);
-      uint8_t* chunk = ds_row + half * (128 * 128);
+      tmem_st_x16(tDP + 16 * ch, ds);
+      if (ch == 0) {
+        // The dS tile's shared memory is free once dV_i has read dO_i (dS
+        // over dO) or dQ_{i-1} has read dS (a tile of its own).
+        if (!bwd_warp_wait(&sb.dv_done, i & 1, status)) return;
+        if (!C::DS_IN_DO && i > 0 && !bwd_warp_wait(&sb.dq_full, (i - 1) & 1, status)) return;
+      }
 #pragma unroll
-      for (int un = 0; un < 8; ++un)
-        *reinterpret_cast<uint4*>(chunk + ((un ^ (t & 7)) << 4)) =
+      for (int un = 0; un < 4; ++un) {
+        const int unit = 4 * ch + un;
+        *reinterpret_cast<uint4*>(ds_row + ((unit ^ (t & 7)) << 4)) =
             make_uint4(ds[4 * un], ds[4 * un + 1], ds[4 * un + 2], ds[4 * un + 3]);
+      }
     }
     fence_proxy_async_smem();
     tmem_st_wait();
@@ -332,55 +370,60 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
     mbar_arrive(&sb.ds_ready);
   }
 
-  // ---- Epilogue: dK and dV rows of this CTA's keys, in the input type.
+  // ---- Epilogue: dK (warpgroup 0) or dV (warpgroup 1) rows of this CTA's
+  // keys, in the input type.
   const bool valid = key < p.Nk;
-  uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.dk) +
-                    2 * ((int64_t)u.b * p.dk_sb + (int64_t)u.hk * p.dk_sh + (int64_t)key * p.dk_sn);
-  uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.dv) +
-                    2 * ((int64_t)u.b * p.dv_sb + (int64_t)u.hk * p.dv_sh + (int64_t)key * p.dv_sn);
+  uint8_t* row = half == 0 ? reinterpret_cast<uint8_t*>(p.dk) +
+                                 2 * ((int64_t)u.b * p.dk_sb + (int64_t)u.hk * p.dk_sh + (int64_t)key * p.dk_sn)
+                           : reinterpret_cast<uint8_t*>(p.dv) +
+                                 2 * ((int64_t)u.b * p.dv_sb + (int64_t)u.hk * p.dv_sh + (int64_t)key * p.dv_sn);
   if (u.steps == 0) {  // no query reads these keys
     if (valid) {
 #pragma unroll
-      for (int c = 0; c < D; c += 8) {
-        *reinterpret_cast<uint4*>(dk_row + 2 * c) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(dv_row + 2 * c) = make_uint4(0u, 0u, 0u, 0u);
-      }
+      for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(row + 2 * c) = make_uint4(0u, 0u, 0u, 0u);
     }
     return;
   }
   if (!bwd_warp_wait(&sb.kv_done, 0, status)) return;
   tc_fence_after();
+  const uint32_t tsrc = tmem + (half == 0 ? C::TM_DK : C::TM_DV) + lane_off;
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const uint32_t tsrc = tmem + (which ? C::TM_DV : C::TM_DK) + lane_off;
-    uint8_t* row = which ? dv_row : dk_row;
+  for (int c = 0; c < D; c += 32) {
+    uint32_t r[32];
+    tmem_ld_x32(tsrc + c, r);
+    tmem_ld_wait32(r);
+    uint32_t w[16];
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t r[32];
-      tmem_ld_x32(tsrc + c, r);
-      tmem_ld_wait32(r);
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = bwd_pack<BF16>(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(row + 2 * c);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-        dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-      }
+    for (int j = 0; j < 16; ++j) w[j] = bwd_pack<BF16>(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(row + 2 * c);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+      dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
     }
   }
 }
 
-// Warps 4-7: thread t owns query row q0 + t of each step's dQ contribution.
+// Warpgroup 2: thread t owns query row q0 + t of each step's dQ contribution.
+// The row is read from tensor memory (which frees it for the next step),
+// then staged 32 columns at a time in a swizzled shared-memory box that one
+// thread adds to the FP32 dQ buffer with a TMA reduce (rows past Nq fall
+// outside the map and are dropped).  The box is handed back and forth on two
+// mbarriers, so every wait is bounded.
 template <int D>
-__device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint32_t tmem, const BwdUnit u, const BwdParams& p) {
+__device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t tmem, const BwdUnit u,
+                                       const BwdParams& p, const CUtensorMap* tmDQ) {
   using C = BwdCfg<D>;
   const int t = threadIdx.x & 127;
+  const bool leader = t == 0;
   const uint32_t tS = tmem + C::TM_S + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16);
-  for (int i = 0; i < u.steps; ++i) {
-    if (!bwd_warp_wait(&sb.dq_full, i & 1, p.status)) return;
+  uint8_t* stage_row = smem + C::OFF_STAGE + t * 128;
+  int box = 0;  // boxes staged so far: the phase of stage_free / stage_full
+  bool ok = true;
+  if (leader) mbar_arrive(&sb.stage_free);
+  for (int i = 0; i < u.steps && ok; ++i) {
+    if (!bwd_warp_wait(&sb.dq_full, i & 1, p.status)) break;
     tc_fence_after();
     uint32_t r[D];
 #pragma unroll
@@ -390,23 +433,40 @@ __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint32_t tmem, const Bwd
     for (int c = 32; c < D; c += 32) fence_regs32(r + c);
     tc_fence_before();
     mbar_arrive(&sb.dq_empty);
-    const int q = u.q0(i) + t;
-    if (q < p.Nq) {
-      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)u.b * p.Hq + u.head(i)) * p.Nq + q) * D);
+    const int h = u.head(i), q0 = u.q0(i);
 #pragma unroll
-      for (int c = 0; c < D / 4; ++c)
-        atomicAdd(dst + c, make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                       __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])));
+    for (int c = 0; c < D && ok; c += 32, ++box) {
+      if (!bwd_warp_wait(&sb.stage_free, box & 1, p.status)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int un = 0; un < 8; ++un)
+        *reinterpret_cast<uint4*>(stage_row + ((un ^ (t & 7)) << 4)) =
+            make_uint4(r[c + 4 * un], r[c + 4 * un + 1], r[c + 4 * un + 2], r[c + 4 * un + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(&sb.stage_full);
+      if (leader) {
+        if (!mbar_wait(&sb.stage_full, box & 1, p.status)) {
+          ok = false;  // the other threads leave at their next bounded wait
+          break;
+        }
+        tma_reduce_add_3d(tmDQ, smem + C::OFF_STAGE, c, q0, u.b * p.Hq + h);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the box has left shared memory
+        mbar_arrive(&sb.stage_free);
+      }
     }
   }
+  if (leader) bulk_wait_all();
 }
 
 // Grid: x = key block, y = key/value head, z = batch.
 template <int D, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   __shared__ BwdBarriers sb;
   extern __shared__ uint8_t smem_raw[];
@@ -434,16 +494,19 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sb.q_full[s], 1);
       mbar_init(&sb.q_empty[s], 1);
+      mbar_init(&sb.do_full[s], 1);
+      mbar_init(&sb.do_empty[s], 1);
     }
-    mbar_init(&sb.do_full, 1);
-    mbar_init(&sb.do_empty, 1);
+    mbar_init(&sb.dv_done, 1);
     mbar_init(&sb.s_full, 1);
     mbar_init(&sb.dp_full, 1);
-    mbar_init(&sb.p_ready, 128);
-    mbar_init(&sb.ds_ready, 128);
+    mbar_init(&sb.p_ready, 256);
+    mbar_init(&sb.ds_ready, 256);
     mbar_init(&sb.dq_full, 1);
     mbar_init(&sb.dq_empty, 128);
     mbar_init(&sb.kv_done, 1);
+    mbar_init(&sb.stage_free, 1);
+    mbar_init(&sb.stage_full, 128);
     fence_mbar_init();
   }
   if (warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0) {
@@ -451,6 +514,7 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQ);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
@@ -461,18 +525,22 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = sb.tmem_base;
 
-  if (warp < 4) {
-    bwd_compute<D, BF16>(sb, smem, tmem, u, p);
-  } else if (warp < 8) {
-    bwd_dq<D>(sb, tmem, u, p);
-  } else if (u.steps > 0) {
-    const bool lane0 = (threadIdx.x & 31) == 0;
-    if (warp == C::PRODUCER_WARP) {
-      if (lane0) bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, sb, smem, u, p);
-      __syncwarp();
-    } else if (warp == C::MMA_WARP) {
-      if (lane0) bwd_mma<D>(sb, smem, tmem, u, BF16 ? 1u : 0u, p.status);
-      __syncwarp();
+  if (warp < 8) {
+    bwd_compute<D, BF16>(sb, smem, tmem, u, p, warp >> 2);
+  } else if (warp < 12) {
+    regs_grow<C::DQ_REGS>();
+    bwd_dq<D>(sb, smem, tmem, u, p, &tmDQ);
+  } else {
+    regs_shrink<C::CTRL_REGS>();
+    if (u.steps > 0) {
+      const bool lane0 = (threadIdx.x & 31) == 0;
+      if (warp == C::PRODUCER_WARP) {
+        if (lane0) bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, sb, smem, u, p);
+        __syncwarp();
+      } else if (warp == C::MMA_WARP) {
+        if (lane0) bwd_mma<D>(sb, smem, tmem, u, BF16 ? 1u : 0u, p.status);
+        __syncwarp();
+      }
     }
   }
   tc_fence_before();

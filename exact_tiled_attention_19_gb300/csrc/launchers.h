@@ -53,8 +53,9 @@ struct BwdPreParams {
   int64_t do_sb, do_sh, do_sn;
   int64_t rows;                  // B * Hq * Nq_pad
   int Hq, Nq, Nq_pad;
-  float* dvec;                   // out: [B * Hq][Nq_pad]
-  float* lse2;                   // out: [B * Hq][Nq_pad]
+  float scale;
+  float* nsd;                    // out: [B * Hq][Nq_pad], -scale * <dO, O>
+  float* nlse2;                  // out: [B * Hq][Nq_pad], -lse * log2(e)
   float* dq_acc;                 // out: [B, Hq, Nq, D] zeroed
 };
 
@@ -72,7 +73,7 @@ cudaError_t launch_bwd_convert(int D, bool bf16, const BwdConvertParams& c, cuda
 
 #define ETATTN_DECLARE_BWD_LAUNCHER(name)                                                                  \
   cudaError_t name(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout, \
-                   const BwdParams& p, dim3 grid, cudaStream_t stream);
+                   const CUtensorMap& dq_acc, const BwdParams& p, dim3 grid, cudaStream_t stream);
 
 ETATTN_DECLARE_BWD_LAUNCHER(launch_bwd_d32_0)
 ETATTN_DECLARE_BWD_LAUNCHER(launch_bwd_d32_1)

@@ -100,6 +100,26 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// 3-D tiled reduce-add of one box from shared memory into global memory
+// (element-wise add, performed at L2); tracked as a bulk async group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has finished reading
+// its shared-memory source (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Barrier among `count` threads (a multiple of 32) on named barrier `id`.
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Make this thread's ordinary shared-memory stores visible to the async
 // proxy (TMA and the tensor core read shared memory through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -221,6 +241,7 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void fence_regs32(uint32_t* r) {
   asm volatile("" : ETATTN_RW8(r, 0), ETATTN_RW8(r, 8), ETATTN_RW8(r, 16), ETATTN_RW8(r, 24));
 }
+__device__ __forceinline__ void fence_regs16(uint32_t* r) { asm volatile("" : ETATTN_RW8(r, 0), ETATTN_RW8(r, 8)); }
 
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
