@@ -38,7 +38,8 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; µs/call (1 GPU)
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PER_CONFIG = ["n129_d32_f16_causal", "n512_d64_f16_causal", "n512_d64_f16_noncausal", "n512_d64_f16_causal_qx30",
               "b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd", "gqa_b2_h32x8_n8192_d128_bf16",
-              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384", "decode_b8_h32x8_k32768"]
+              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384", "decode_b8_h32x8_k32768",
+              "bwd_b4_h16_n4096_d128_bf16", "bwd_gqa_b2_h32x8_n8192_d128_bf16"]
 
 
 def parse_args():
@@ -193,6 +194,20 @@ def device_inputs(w, device):
     else:
         dev["o"] = torch.empty((w.B, w.Hq, w.N, w.D), dtype=w.dtype, device=device)
         dev["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=device)
+    if w.backward:
+        from exact_tiled_attention_19_gb300 import binding
+        g = torch.Generator().manual_seed(1)
+        inp["dout"] = torch.randn(inp["q"].shape, generator=g, dtype=torch.float32).to(w.dtype)
+        dev["dout"] = inp["dout"].to(device)
+        win = dict(window_left=w.window_left, window_right=w.window_right)
+        binding.attention(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale, out=dev["o"],
+                          lse=dev["lse"], **win)
+        dev["dq"] = torch.empty_like(dev["q"])
+        dev["dk"] = torch.empty_like(dev["k"])
+        dev["dv"] = torch.empty_like(dev["v"])
+        dev["ws"] = torch.empty(max(binding.attn_bwd_workspace_size(w.B, w.Hq, w.N, w.D), 1), dtype=torch.uint8,
+                                device=device)
+        torch.cuda.synchronize()
     if w.splitkv:
         from exact_tiled_attention_19_gb300 import binding
         rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.Hkv, w.N, w.keys)
@@ -204,7 +219,10 @@ def device_inputs(w, device):
 
 
 def launches_per_call(w):
-    """Kernels one call launches: the split-KV path adds the merge launch."""
+    """Kernels one call launches: the split-KV path adds the merge launch,
+    the backward pass a launch before (row statistics) and after (dQ)."""
+    if w.backward:
+        return 3
     return 2 if w.splitkv and w.keys > 0 else 1
 
 
@@ -219,6 +237,11 @@ def make_call(w, dev, stream):
         def call():
             binding.attention_varlen(dev["q"], dev["k"], dev["v"], dev["cu"], max(w.seqlens), causal=w.causal,
                                      scale=w.scale, out=dev["o"], lse=dev["lse"], stream=stream, **kw, **win)
+    elif w.backward:
+        def call():
+            binding.attention_backward(dev["q"], dev["k"], dev["v"], dev["o"], dev["lse"], dev["dout"],
+                                       causal=w.causal, scale=w.scale, dq=dev["dq"], dk=dev["dk"], dv=dev["dv"],
+                                       workspace=dev["ws"], stream=stream, **win)
     elif w.splitkv:
         def call():
             binding.attention_splitkv(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale,
@@ -265,8 +288,8 @@ def time_e2e(w, inp, dev, stream, K, W, world):
     and copies O and lse back."""
     import torch
     from exact_tiled_attention_19_gb300 import binding
-    if not w.square:
-        return None  # the host-buffer entry points take equal query/key lengths without a window
+    if not w.square or w.backward or w.splitkv:
+        return None  # the host-buffer entry points run the plain forward pass
     pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
     o_h = torch.empty(dev["o"].shape, dtype=w.dtype).pin_memory()
     l_h = torch.empty(dev["lse"].shape, dtype=torch.float32).pin_memory()
@@ -344,13 +367,16 @@ def oracle_sample(w):
         desc = f"sequence {s} (L={L}) of the packed batch, all {w.Hq} heads"
         flops = 4.0 * L * L * w.D * len(heads) / (2 if w.causal else 1)
         return desc, probs, flops
-    del g
     inp = W.make_inputs(w)
     heads = list(range(min(2, w.Hq)))
     probs = []
+    dout = torch.randn(inp["q"].shape, generator=g, dtype=torch.float32).to(w.dtype) if w.backward else None
     for h in heads:
         hk = h // (w.Hq // w.Hkv)
-        probs.append(tuple(inp[n][0, hh].float().double().numpy() for n, hh in (("q", h), ("k", hk), ("v", hk))))
+        prob = tuple(inp[n][0, hh].float().double().numpy() for n, hh in (("q", h), ("k", hk), ("v", hk)))
+        if w.backward:
+            prob = prob + (dout[0, h].float().double().numpy(),)
+        probs.append(prob)
     desc = f"batch 0, query heads {heads}, all {w.N} rows"
     flops = head_flops(w) * len(heads)
     return desc, probs, flops
@@ -359,14 +385,17 @@ def oracle_sample(w):
 def head_flops(w):
     """The metric's FLOPs of one (sequence, query head) of a batched workload
     (every one is the same size)."""
-    return w.flops_convention() / (w.B * w.Hq)
+    return w.flops() / (w.B * w.Hq)
 
 
 def run_oracle_problem(prob, w):
     import oracle
+    win = dict(window_left=w.window_left, window_right=w.window_right)
+    if w.backward:
+        q, k, v, do = (x[None, None] for x in prob)
+        return oracle.attention_backward_dense(q, k, v, do, causal=w.causal, scale=w.scale, **win)
     q, k, v = prob
-    return oracle.attention_rows(q, k, v, np.arange(q.shape[0]), causal=w.causal, scale=w.scale,
-                                 window_left=w.window_left, window_right=w.window_right)
+    return oracle.attention_rows(q, k, v, np.arange(q.shape[0]), causal=w.causal, scale=w.scale, **win)
 
 
 def cpu_baseline(w):
@@ -431,6 +460,8 @@ def correctness_gate(w, inp, dev):
     import torch
     tol = 2e-3 if w.dtype == torch.float16 else 1e-2
     f64 = lambda t: t.float().double().cpu().numpy()
+    if w.backward:
+        return backward_gate(w, inp, dev, f64)
     o, lse = dev["o"], dev["lse"]
     if not bool(torch.isfinite(o).all()) or not bool(torch.isfinite(lse).all()):
         return False, float("inf")
@@ -459,6 +490,28 @@ def correctness_gate(w, inp, dev):
             worst = max(worst, float(np.max(np.abs(f64(o[b, h][rows]) - ro))),
                         float(np.max(np.abs(f64(lse[b, h][rows]) - rl))))
     return worst <= tol, worst
+
+
+def backward_gate(w, inp, dev, f64):
+    """Sampled rows of (batch 0, KV head 0) of dQ, dK, dV against the oracle,
+    each element within u |G| + 8 u M (M the sum of the absolute values of
+    its terms, u the input type's half-ulp), as in the GPU parity tests.
+    Returns (ok, worst error / bound)."""
+    import oracle
+    import torch
+    u = 2.0 ** -9 if w.dtype == torch.bfloat16 else 2.0 ** -12
+    g = w.Hq // w.Hkv
+    rows = np.array(sorted({0, 1, 127, 128, w.N // 2, w.N - 1}))
+    out = oracle.attention_backward_sampled(f64(inp["q"][0, :g]), f64(inp["k"][0, 0]), f64(inp["v"][0, 0]),
+                                            f64(inp["dout"][0, :g]), rows, rows, causal=w.causal, scale=w.scale,
+                                            group=g, window_left=w.window_left, window_right=w.window_right,
+                                            magnitudes=True)
+    gpu = (f64(dev["dq"][0, :g])[:, rows], f64(dev["dk"][0, 0])[rows], f64(dev["dv"][0, 0])[rows])
+    worst = 0.0
+    for got, ref, mag in zip(gpu, out[:3], out[3:]):
+        bound = u * np.abs(ref) + 8 * u * mag + 1e-6 * max(float(mag.max()), 1e-30)
+        worst = max(worst, float((np.abs(got - ref) / bound).max()))
+    return worst <= 1.0, worst
 
 
 def microbench(w, call, stream, samples=7, calls=20, warm=5):
@@ -513,7 +566,7 @@ def per_config_report(stream, device, peaks):
             with torch.cuda.stream(stream):
                 m = microbench(w, call, stream)
             us = m["us_graph_median"]
-            tf = w.flops_convention() / (us * 1e-6) / 1e12
+            tf = w.flops() / (us * 1e-6) / 1e12
             entry.update({k: round(v, 3) for k, v in m.items()})
             entry["tflops_graph"] = round(tf, 2)
             entry["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
@@ -561,7 +614,7 @@ def main():
     with torch.cuda.stream(stream):
         total_ms, per_launch, clocks = time_steps(call, stream, args.steps, max(3, args.warmup), world, sampler)
     total_ms = max_over_ranks(total_ms, world)
-    flops = w.flops_convention()
+    flops = w.flops()
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     launch_ms = statistics.mean(per_launch)
     achieved = flops / (launch_ms * 1e-3) / 1e12

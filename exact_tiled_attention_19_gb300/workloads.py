@@ -53,6 +53,7 @@ class Workload:
     window_left: int = -1         # local window (keys before the row's key position); -1 = none
     window_right: int = -1
     splitkv: bool = False         # run through the split-KV entry point (few queries, many keys)
+    backward: bool = False        # the backward pass (dQ, dK, dV for a seeded upstream gradient)
 
     @property
     def scale(self) -> float:
@@ -90,6 +91,12 @@ class Workload:
         f = sum(4.0 * lq * lk * self.D for lq, lk in self.lengths()) * self.Hq
         return f / 2 if self.causal else f
 
+    def flops(self) -> float:
+        """The FLOPs a call is credited with: the forward convention, times
+        2.5 for the backward pass (five products of the forward's size
+        instead of two: S, dP, dV, dK, dQ)."""
+        return self.flops_convention() * (2.5 if self.backward else 1.0)
+
     def eligible_pairs(self) -> int:
         """(query row, key) pairs that enter the softmax, per query head,
         summed over sequences.  Query row r of Lq sits at key position
@@ -119,13 +126,16 @@ class Workload:
     def memory_bound(self) -> bool:
         """Below about 64 FLOP per algorithmic byte the HBM, not the tensor
         core, bounds the call (the GB300 ridge point is near 280)."""
-        return self.flops_convention() < 64 * self.io_bytes()
+        return self.flops() < 64 * self.io_bytes()
 
     def io_bytes(self) -> int:
-        """Algorithmic HBM bytes of one call: read Q, K, V once, write O and
-        the FP32 logsumexp once."""
+        """Algorithmic HBM bytes of one call.  Forward: read Q, K, V once,
+        write O and the FP32 logsumexp once.  Backward: read Q, K, V, O, dO
+        and lse once, write dQ, dK, dV once."""
         esz = torch.tensor([], dtype=self.dtype).element_size()
         tq, tk = self.total_tokens, self.total_keys
+        if self.backward:
+            return (4 * tq * self.Hq * self.D + 4 * tk * self.Hkv * self.D) * esz + tq * self.Hq * 4
         return (2 * tq * self.Hq * self.D + 2 * tk * self.Hkv * self.D) * esz + tq * self.Hq * 4
 
 
@@ -155,6 +165,11 @@ WORKLOADS = dict([
            "causal), D=128, BF16", 2, 32, 8, 2048, 128, BF16, True, Nk=16384),
     _named("window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys (diagonal included), D=128, "
            "BF16", 2, 16, 16, 16384, 128, BF16, True, window_left=4095),
+    # The backward pass of two forward workloads.
+    _named("bwd_b4_h16_n4096_d128_bf16", "backward: B=4, H=16, N=4096, D=128, BF16, causal, [B,H,N,D]", 4, 16, 16,
+           4096, 128, BF16, True, backward=True),
+    _named("bwd_gqa_b2_h32x8_n8192_d128_bf16", "backward: GQA B=2, Hq=32, Hkv=8, N=8192, D=128, BF16, causal", 2,
+           32, 8, 8192, 128, BF16, True, backward=True),
     # Few queries over many keys: split-KV.
     _named("decode_b8_h32x8_k32768", "decode step: GQA B=8, Hq=32, Hkv=8, 1 query over 32768 keys, D=128, BF16, "
            "split-KV", 8, 32, 8, 1, 128, BF16, True, Nk=32768, splitkv=True),
