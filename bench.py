@@ -145,26 +145,32 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def kernel_source_digest():
+KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd_kernel.cuh", "sm103_ptx.cuh"),
+                  "attn_bwd_kernel": ("attn_bwd_kernel.cuh", "sm103_ptx.cuh")}
+
+
+def kernel_source_digest(kernel: str = "attn_fwd_kernel"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_19_gb300", "csrc")
-    for name in ("attn_fwd_kernel.cuh", "sm103_ptx.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+def measured_traffic(w):
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu summary, if it was taken on the current kernel source;
+    else None."""
+    kernel = "attn_bwd_kernel" if w.backward else "attn_fwd_kernel"
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            d = json.load(f)
+            d = json.load(f).get("kernels", {}).get(kernel, {})
     except (OSError, ValueError):
         return None
-    if d.get("kernel_source_sha256") != kernel_source_digest():
+    if d.get("source_sha256") != kernel_source_digest(kernel):
         return None
-    entry = d.get("workloads", {}).get(workload)
+    entry = d.get("workloads", {}).get(w.name)
     return None if entry is None else entry.get("dram_bytes_per_launch")
 
 
@@ -643,7 +649,7 @@ def main():
     if w.memory_bound:
         gbs = w.io_bytes() / (launch_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic(w.name),
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": measured_traffic(w),
                     "peak_source": "HBM copy, measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                     else "HBM copy, fallback",
                     "algorithmic_bytes_per_launch": w.io_bytes(), "algorithmic_flops_per_launch": flops,
@@ -653,7 +659,7 @@ def main():
     else:
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                    "traffic": measured_traffic(w.name),
+                    "traffic": measured_traffic(w),
                     "peak_source": f"bf16 dense burst, {peak_src} (MEASURED_PEAKS.json)"
                     if peak_src == "measured" else "bf16 dense burst, fallback",
                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
