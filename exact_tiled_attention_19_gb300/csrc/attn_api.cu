@@ -203,25 +203,33 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
 //
 // With grouped-query packing (p.qpack = P > 1) `tokens` counts rows (query
 // tokens x P) and gy head packs; such launches use one sub-tile per CTA.
+//
+// A problem whose 128-row blocks fill at most half the SMs and whose rows
+// read more than one key tile (`key_tiles`, the most any row block streams)
+// runs the key-split build instead: one row block per CTA, its two
+// sub-tiles taking alternate key tiles.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, bool general,
-                   cudaStream_t s) {
+                   cudaStream_t s, int64_t key_tiles = 0) {
   const bool bf = dtype == ETATTN_BF16;
   const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
-  const int64_t blocks2 = (tokens + 255) / 256;
+  const int64_t blocks1 = (tokens + 127) / 128, blocks2 = (tokens + 255) / 256;
+  const bool ksplit = splits == 1 && p.qpack == 1 && key_tiles >= 2 && 2 * blocks1 * (int64_t)gy * gz <= num_sms;
   // Up to 128 query rows fill one sub-tile: a second one would only idle.
   const int nsub = (p.qpack > 1 || tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
-  const int64_t gx = (nsub == 2 ? blocks2 : (tokens + 127) / 128) * splits;
+  const int64_t gx = (ksplit || nsub == 1 ? blocks1 : blocks2) * splits;
   if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const dim3 g((unsigned)gx, gy, gz);
   switch (D) {
     case 32:
-      return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, general, s) : launch_fwd_d32_0(q, k, v, p, g, nsub, general, s);
+      return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, general, ksplit, s)
+                : launch_fwd_d32_0(q, k, v, p, g, nsub, general, ksplit, s);
     case 64:
-      return bf ? launch_fwd_d64_1(q, k, v, p, g, nsub, general, s) : launch_fwd_d64_0(q, k, v, p, g, nsub, general, s);
+      return bf ? launch_fwd_d64_1(q, k, v, p, g, nsub, general, ksplit, s)
+                : launch_fwd_d64_0(q, k, v, p, g, nsub, general, ksplit, s);
     default:
-      return bf ? launch_fwd_d128_1(q, k, v, p, g, nsub, general, s)
-                : launch_fwd_d128_0(q, k, v, p, g, nsub, general, s);
+      return bf ? launch_fwd_d128_1(q, k, v, p, g, nsub, general, ksplit, s)
+                : launch_fwd_d128_0(q, k, v, p, g, nsub, general, ksplit, s);
   }
 }
 
@@ -451,7 +459,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.split_tiles = (key_tiles + split->num_splits - 1) / split->num_splits;
   }
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)Nq * qpack, (unsigned)(Hq / qpack), (unsigned)B, num_sms,
-                         general, st);
+                         general, st, (Nk + 127) / 128);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splitting) {
     CombineParams c{};
@@ -747,7 +755,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   p.qpack = qpack;
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)max_seqlen_q * qpack, (unsigned)(Hq / qpack),
-                         (unsigned)num_seqs, num_sms, general, static_cast<cudaStream_t>(stream));
+                         (unsigned)num_seqs, num_sms, general, static_cast<cudaStream_t>(stream),
+                         ((int64_t)max_seqlen_k + 127) / 128);
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }

@@ -23,11 +23,11 @@ namespace etattn {
 
 namespace {
 
-template <int NSUB, bool GEN>
+template <int NSUB, bool GEN, bool KS>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p, dim3 grid,
                        cudaStream_t stream) {
   using C = TileCfg<ETATTN_INST_D, NSUB>;
-  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0, GEN>;
+  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0, GEN, KS>;
   // The dynamic shared-memory opt-in is per device; set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -55,10 +55,13 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 }  // namespace
 
 cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
-                            dim3 grid, int nsub, bool general, cudaStream_t stream) {
+                            dim3 grid, int nsub, bool general, bool ksplit, cudaStream_t stream) {
+  if (ksplit) return launch_one<2, true, true>(q, k, v, p, grid, stream);
   if (general)
-    return nsub == 1 ? launch_one<1, true>(q, k, v, p, grid, stream) : launch_one<2, true>(q, k, v, p, grid, stream);
-  return nsub == 1 ? launch_one<1, false>(q, k, v, p, grid, stream) : launch_one<2, false>(q, k, v, p, grid, stream);
+    return nsub == 1 ? launch_one<1, true, false>(q, k, v, p, grid, stream)
+                     : launch_one<2, true, false>(q, k, v, p, grid, stream);
+  return nsub == 1 ? launch_one<1, false, false>(q, k, v, p, grid, stream)
+                   : launch_one<2, false, false>(q, k, v, p, grid, stream);
 }
 
 }  // namespace etattn

@@ -33,6 +33,15 @@
 // few-query call (a decode step) streams each K/V tile once for the group and
 // fills P times more of the tile.
 //
+// Key split (KS, for problems too small to fill the GPU): both sub-tiles
+// hold the same 128 query rows and take alternate key tiles (even / odd), so
+// the two softmax chains of a CTA take turns on the tensor core instead of
+// running one after the other; at the end sub-tile 1 hands its (m, l) to
+// sub-tile 0 through shared memory and its O through tensor memory, and
+// sub-tile 0 merges the two states ("Attention algorithms and data
+// movement", lesson 01: merging normalised partial states) and writes the
+// rows.
+//
 // A CTA owns 256 query rows as two sub-tiles (rows [0,128) and [128,256) of
 // the block).  Both read the same K/V tiles from shared memory.
 //
@@ -155,6 +164,8 @@ struct SmemBarriers {
   uint64_t s_full[2];            // per sub-tile: S_s(j) is in tensor memory (and PV_s(j-1) is done)
   uint64_t p_full[2];            // per sub-tile: P_s(j) written and O_s corrected
   uint64_t o_done[2];            // per sub-tile: last PV_s has completed
+  uint64_t merge_ready;          // key split: sub-tile 1's (m, l) and O are final (128 arrivals)
+  float merge_m[128], merge_l[128];  // key split: sub-tile 1's running max and sum per row
   uint32_t tmem_base;
 };
 
@@ -191,24 +202,29 @@ __device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit&
 // ----------------------------------------------------------------- producer
 // Runs on one thread.  (Waits are single-thread too: 32 lanes polling one
 // mbarrier serialise on it and cost more than a tile's MMA issue slot.)
-template <int D, int NSUB>
+// Loads Q and key tiles j_from .. n_tot - 1 (with j_from = 0 the Q tiles
+// too).  The first call, with j_to = 1, runs before the CTA's first barrier:
+// the Q and first K / V tiles are then in flight while tensor memory is
+// allocated; every later slot may still be in use and is waited for.
+template <int D, int NSUB, bool KS>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, SmemBarriers& sb, uint8_t* smem,
-                                              const Unit u, int hn_swapped, int* status) {
+                                              const Unit u, int hn_swapped, int* status, int j_from, int j_to) {
   using C = TileCfg<D, NSUB>;
+  constexpr int NQ = KS ? 1 : NSUB;  // Q tiles: the key split's sub-tiles share their rows
   const bool swq = hn_swapped & 1, swk = (hn_swapped >> 1) & 1, swv = (hn_swapped >> 2) & 1;
   if (u.n_tot == 0) return;  // no row of this CTA reads a key
-  {
-    mbar_arrive_expect_tx(&sb.q_full, NSUB * C::Q_BYTES);
+  if (j_from == 0) {
+    mbar_arrive_expect_tx(&sb.q_full, NQ * C::Q_BYTES);
 #pragma unroll
-    for (int s = 0; s < NSUB; ++s)
+    for (int s = 0; s < NQ; ++s)
 #pragma unroll
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_Q + s * C::Q_BYTES + c * C::BM * C::SW_BYTES, tmQ, &sb.q_full,
                       c * C::SW_ELEMS, u.tok0q + u.row0 + s * u.span, u.h, u.bcoord, swq);
   }
-  int ks = 0, kph = 0;  // K ring slot and its phase for tile j
-  for (int j = 0; j < u.n_tot; ++j) {
+  int ks = j_from % C::K_STAGES, kph = (j_from / C::K_STAGES) & 1;  // K ring slot and its phase for tile j
+  for (int j = j_from; j < min(j_to, u.n_tot); ++j) {
     const int key0 = u.tok0k + (u.kt0 + j) * C::BN;
     // K_j goes to slot j % 3, whose previous tile j-3 must have been released.
     if (j >= C::K_STAGES && !mbar_wait(&sb.k_empty[ks], kph ^ 1, status)) return;
@@ -285,24 +301,57 @@ __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int 
 // cycle the issuing thread spends elsewhere between groups is idle tensor time.
 // GEN = false is the square, window-free case, where both sub-tiles start at
 // streamed tile 0 and the per-tile range tests fold away at compile time.
-template <int D, int NSUB, bool GEN>
+template <int D, int NSUB, bool GEN, bool KS>
 __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
   using C = TileCfg<D, NSUB>;
   MmaDescs md;
   md.q0 = smem_desc(smem_u32(smem + C::OFF_Q), 16, C::SBO, C::SWIZZLE);
-  md.q1 = md.q0 + (uint64_t)(C::Q_BYTES >> 4);
+  md.q1 = KS ? md.q0 : md.q0 + (uint64_t)(C::Q_BYTES >> 4);
   md.k0 = smem_desc(smem_u32(smem + C::OFF_K), 16, C::SBO, C::SWIZZLE);
   md.k1 = md.k0 + (uint64_t)(C::KV_BYTES >> 4);
   md.k2 = md.k1 + (uint64_t)(C::KV_BYTES >> 4);
   md.v0 = smem_desc(smem_u32(smem + C::OFF_V), C::BN * C::SW_BYTES, C::SBO, C::SWIZZLE);
   md.v1 = md.v0 + (uint64_t)(C::KV_BYTES >> 4);
   // Sub-tile `sub` reads streamed tile j; its own count of that tile.
-  auto reads = [&](int sub, int j) { return GEN ? u.reads(sub, j) : j < u.n(sub); };
-  auto own = [&](int sub, int j) { return GEN ? j - u.f(sub) : j; };
+  // Key split: sub-tile s reads the streamed tiles j = s mod 2.
+  auto reads = [&](int sub, int j) {
+    return KS ? ((j & 1) == sub && j < u.n_tot) : (GEN ? u.reads(sub, j) : j < u.n(sub));
+  };
+  auto own = [&](int sub, int j) { return KS ? j >> 1 : (GEN ? j - u.f(sub) : j); };
   if (u.n_tot == 0) return;  // no row of this CTA reads a key
   if (!mbar_wait(&sb.q_full, 0, status)) return;
 
+  if constexpr (KS) {
+    // Key split: sub-tile s owns the streamed tiles t = 2 jl + s.  Step jl
+    // issues PV_0(jl-1), S_0(jl), PV_1(jl-1), S_1(jl), so the two chains
+    // take turns on the tensor core as the two sub-tiles of a regular CTA
+    // do.  K tile t sits in ring slot t mod 3 (phase t / 3), V tile t in
+    // slot t mod 2 (phase t / 2).
+    for (int jl = 0; jl <= u.n0; ++jl) {
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int tp = 2 * (jl - 1) + sub;  // tile whose PV product is issued now
+        if (jl > 0 && tp < u.n_tot) {
+          if (!mbar_wait(&sb.v_full[tp & 1], (tp >> 1) & 1, status) ||
+              !mbar_wait(&sb.p_full[sub], (jl - 1) & 1, status))
+            return;
+          tc_fence_after();
+          issue_pv<D, NSUB>(md, tmem, sub, tp & 1, jl > 1, idesc_pv);
+          if (jl - 1 == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
+          mma_commit(&sb.v_empty[tp & 1]);
+        }
+        const int tn = 2 * jl + sub;  // tile whose S product is issued now
+        if (tn < u.n_tot) {
+          if (!mbar_wait(&sb.k_full[tn % C::K_STAGES], (tn / C::K_STAGES) & 1, status)) return;
+          tc_fence_after();
+          issue_s<D, NSUB>(md, tmem, sub, tn % C::K_STAGES, idesc_s);
+          mma_commit(&sb.s_full[sub]);
+          mma_commit(&sb.k_empty[tn % C::K_STAGES]);
+        }
+      }
+    }
+  } else {
   int ks = 0, kph = 0;  // K ring slot / phase of the next key tile
   if (!mbar_wait(&sb.k_full[0], 0, status)) return;
   tc_fence_after();
@@ -345,6 +394,7 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
       }
     }
   }
+  }
   // Drain: wait for the commit arrivals nobody else consumes (the last
   // tiles' ring releases and the final PV of each sub-tile) so that no
   // arrival can land in shared memory after the CTA exits.
@@ -373,7 +423,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // GEN = false is the square, window-free case: every row reads key 0 in the
 // first tile, so no row meets a tile with m = -inf and no lower edge exists.
-template <int D, int NSUB, bool BF16, bool GEN>
+template <int D, int NSUB, bool BF16, bool GEN, bool KS>
 __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, const FwdParams& p, const Unit u,
                                              int s) {
   using C = TileCfg<D, NSUB>;
@@ -394,7 +444,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     }
   }
   const int head = u.h + hl;
-  const int row_pos = u.row0 + s * u.span + tl;  // logical position inside the query sequence
+  const int row_pos = u.row0 + (KS ? 0 : s * u.span) + tl;  // logical position inside the query sequence
   const bool valid = row_pos < u.Lq;
   // Output row and lse addresses (formed where they are used, so that they
   // hold no registers across the tile loop).
@@ -408,6 +458,12 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   auto part_index = [&]() { return (int64_t)u.split * p.part_stride + lse_index(); };
   auto part_row = [&]() { return p.part_o + part_index() * D; };
   const bool split_mode = GEN && p.part_o != nullptr;
+  if (KS && s == 1 && n == 0) {  // key split, nothing for sub-tile 1: an empty state
+    sb.merge_m[t] = -INFINITY;
+    sb.merge_l[t] = 0.f;
+    mbar_arrive(&sb.merge_ready);
+    return;
+  }
   if (n == 0) {  // no row of this sub-tile may read a key: O = 0, lse = -inf
     if (valid) {
       if (split_mode) {
@@ -487,8 +543,8 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 #pragma unroll
       for (int i = C::BN / 2; i < C::BN; ++i) sv[i] = i > lim_hi ? -INFINITY : sv[i];
     }
-    lim_hi -= C::BN;
-    lim_lo -= C::BN;
+    lim_hi -= (KS ? 2 : 1) * C::BN;  // the key split's sub-tiles take every other tile
+    lim_lo -= (KS ? 2 : 1) * C::BN;
 #pragma unroll
     for (int i = C::BN / 2; i < C::BN; i += 8) {
       mx0 = max3(mx0, sv[i], sv[i + 1]);
@@ -556,6 +612,28 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   // it gets O = 0 and lse = -inf.
   if (!warp_wait(&sb.o_done[s], 0, status)) return;
   tc_fence_after();
+  if (KS && s == 1) {  // hand the state to sub-tile 0
+    sb.merge_m[t] = m_run;
+    sb.merge_l[t] = l_run;
+    tc_fence_before();
+    mbar_arrive(&sb.merge_ready);
+    return;
+  }
+  // Key split: merge sub-tile 1's state into this one, rescaling both to the
+  // larger reference maximum; O_1 is read from sub-tile 1's columns.
+  float w0 = 1.f, w1 = 0.f;
+  if (KS) {
+    if (!warp_wait(&sb.merge_ready, 0, status)) return;
+    tc_fence_after();
+    const float m1 = sb.merge_m[t], l1 = sb.merge_l[t];
+    if (l1 > 0.f) {
+      const float mm = fmaxf(m_run, m1);
+      w0 = l_run > 0.f ? ex2_approx((m_run - mm) * c2) : 0.f;
+      w1 = ex2_approx((m1 - mm) * c2);
+      l_run = l_run * w0 + l1 * w1;
+      m_run = mm;
+    }
+  }
   const bool nonempty = l_run > 0.f;
   const float inv_l = nonempty ? 1.f / l_run : 0.f;
   if (split_mode) {
@@ -580,15 +658,28 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     return;
   }
   uint8_t* orow = o_row();
+  const float s0 = w0 * inv_l, s1 = w1 * inv_l;
 #pragma unroll
   for (int c = 0; c < D; c += 32) {
     uint32_t o[32];
     tmem_ld_x32(tO + c, o);
     tmem_ld_wait32(o);
+    if (KS && u.n1 > 0) {  // + w1 * O_1 (sub-tile 1's accumulator, same lanes; CTA-uniform branch)
+      uint32_t o1[32];
+      tmem_ld_x32(tO + 128 + c, o1);
+      tmem_ld_wait32(o1);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        o[i] = __float_as_uint(fmaf(__uint_as_float(o1[i]), s1, __uint_as_float(o[i]) * s0));
+    } else if (KS) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * s0);
+    }
+    const float sc = KS ? 1.f : inv_l;
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * sc, __uint_as_float(o[2 * i + 1]) * sc);
     if (valid) {
       uint4* dst = reinterpret_cast<uint4*>(orow + c * 2);
       dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -609,7 +700,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 // throughput configuration; NSUB = 1 gives small problems twice as many CTAs.
 // GEN = true handles unequal lengths and windows; the square, window-free
 // case compiles without their per-tile tests (they cost about 3% there).
-template <int D, int NSUB, bool BF16, bool GEN>
+template <int D, int NSUB, bool BF16, bool GEN, bool KS>
 __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -650,10 +741,18 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     u.split = (int)blockIdx.x % p.num_splits;
     block = (int)(gridDim.x / p.num_splits) - 1 - (int)blockIdx.x / p.num_splits;
   }
-  u.row0 = block * NSUB * u.span;
+  u.row0 = block * (KS ? 1 : NSUB) * u.span;
   if (u.row0 >= u.Lq) return;  // uniform across the CTA
   u.delta = u.Lk - u.Lq;
-  {
+  if (KS) {  // one row block; sub-tile s takes the streamed tiles j = s mod 2
+    const int2 r = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN);
+    u.kt0 = r.x;
+    u.n_tot = r.y > r.x ? r.y - r.x : 0;
+    u.f0 = 0;
+    u.f1 = 1;
+    u.n0 = (u.n_tot + 1) / 2;
+    u.n1 = u.n_tot / 2;
+  } else {
     int2 r0 = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN);
     int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + u.span, u.span, u, p, C::BN) : make_int2(0, 0);
     if (GEN && p.part_o != nullptr) {  // keep this slice's key tiles
@@ -670,8 +769,9 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     u.n1 = a1 ? r1.y - r1.x : 0;
   }
   const int warp = threadIdx.x >> 5;
+  const bool producer = warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0;
 
-  if (threadIdx.x == 0) {
+  if (producer) {
     mbar_init(&sb.q_full, 1);
 #pragma unroll
     for (int i = 0; i < C::K_STAGES; ++i) {
@@ -686,12 +786,12 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
       mbar_init(&sb.p_full[i], 128);
       mbar_init(&sb.o_done[i], 1);
     }
+    mbar_init(&sb.merge_ready, 128);
     fence_mbar_init();
-  }
-  if (warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
+    fence_proxy_async_smem();  // the initialised barriers, as the TMA (async proxy) will see them
+    // Q and the first key tile go out before the CTA's barrier (their
+    // slots are free and only this thread has touched the barriers yet).
+    producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
@@ -704,18 +804,18 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
 
   if (warp < 4 * NSUB) {
     if constexpr (NSUB == 2) regs_grow<C::SOFTMAX_REGS>();
-    softmax_role<D, NSUB, BF16, GEN>(sb, tmem, p, u, warp >> 2);
+    softmax_role<D, NSUB, BF16, GEN, KS>(sb, tmem, p, u, warp >> 2);
   } else {
     if constexpr (NSUB == 2) regs_shrink<C::CTRL_REGS>();
     const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp == C::PRODUCER_WARP) {
-      if (lane0) producer_role<D, NSUB>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status);
+      if (lane0) producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 1, 1 << 30);
       __syncwarp();
     } else if (warp == C::MMA_WARP) {
       constexpr uint32_t ab = BF16 ? 1u : 0u;
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
-      if (lane0) mma_role<D, NSUB, GEN>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+      if (lane0) mma_role<D, NSUB, GEN, KS>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
       __syncwarp();
     }
   }

@@ -10,7 +10,7 @@ import torch
 
 from exact_tiled_attention_19_gb300 import binding
 from exact_tiled_attention_19_gb300 import workloads as W
-from tests.parity_helpers import rebuild_strided, run_gpu
+from tests.parity_helpers import LSE_TOL, O_TOL, rebuild_strided, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -60,19 +60,36 @@ def test_gqa_equals_repeated_kv_bit_identical():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_varlen_equals_per_sequence_calls_bit_identical():
-    lengths = [300, 1, 129, 0, 512]
-    inp = W.random_varlen(lengths, 4, 2, 128, torch.bfloat16, seed=10)
+def _packed_vs_per_sequence(lengths, Hq, Hkv, seed):
+    inp = W.random_varlen(lengths, Hq, Hkv, 128, torch.bfloat16, seed=seed)
     o, lse = run_gpu(inp, True)
     cu = inp["cu_seqlens"].tolist()
+    pairs = []
     for s, L in enumerate(lengths):
         if L == 0:
             continue
         t0 = cu[s]
         per = {n: inp[n][t0:t0 + L].permute(1, 0, 2).unsqueeze(0) for n in ("q", "k", "v")}
         o_s, l_s = run_gpu({n: t.contiguous() for n, t in per.items()}, True)
-        assert torch.equal(o_s[0].permute(1, 0, 2), o[t0:t0 + L])
-        assert torch.equal(l_s[0], lse[:, t0:t0 + L])
+        pairs.append(((o_s[0].permute(1, 0, 2), o[t0:t0 + L]), (l_s[0], lse[:, t0:t0 + L])))
+    return pairs
+
+
+def test_varlen_equals_per_sequence_calls_bit_identical():
+    """Packed and per-sequence calls that run the same kernel build (enough
+    heads that neither is a small problem) give identical bits: every row's
+    arithmetic is the same whatever else shares the launch."""
+    for (a, b), (la, lb) in _packed_vs_per_sequence([300, 1, 129, 0, 512], 80, 20, seed=10):
+        assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_small_problems_agree_with_packed_calls_within_tolerance():
+    """Small per-sequence calls run the key-split build (each row's keys as
+    two partial states merged at the end), so they round differently from
+    the packed call; they agree within the stated tolerance."""
+    for (a, b), (la, lb) in _packed_vs_per_sequence([300, 1, 129, 0, 512], 4, 2, seed=10):
+        assert float((a.float() - b.float()).abs().max()) <= O_TOL[torch.bfloat16]
+        assert float((la - lb).abs().max()) <= LSE_TOL
 
 
 def test_inputs_unchanged_and_deterministic():
