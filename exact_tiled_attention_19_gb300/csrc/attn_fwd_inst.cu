@@ -48,8 +48,20 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the launch may be scheduled while the
+  // previous grid on the stream finishes; the kernel's griddepcontrol.wait
+  // keeps every memory access after that grid's completion.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
 }
 
 }  // namespace

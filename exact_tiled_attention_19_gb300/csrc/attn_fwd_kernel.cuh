@@ -709,6 +709,43 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+  // The next launch on the stream may be scheduled now.  Barrier set-up and
+  // the tensor-memory allocation touch no global memory and run before this
+  // grid waits for the previous one (whose outputs may be its inputs, or
+  // whose inputs its outputs); everything after the wait may read and write.
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5;
+  const bool producer = warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0;
+  if (producer) {
+    mbar_init(&sb.q_full, 1);
+#pragma unroll
+    for (int i = 0; i < C::K_STAGES; ++i) {
+      mbar_init(&sb.k_full[i], 1);
+      mbar_init(&sb.k_empty[i], 1);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.v_full[i], 1);
+      mbar_init(&sb.v_empty[i], 1);
+      mbar_init(&sb.s_full[i], 1);
+      mbar_init(&sb.p_full[i], 128);
+      mbar_init(&sb.o_done[i], 1);
+    }
+    mbar_init(&sb.merge_ready, 128);
+    fence_mbar_init();
+    fence_proxy_async_smem();  // the initialised barriers, as the TMA (async proxy) will see them
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  pdl_wait();
+
+  // The CTA's work; `active` is uniform across the CTA.
+  bool active = true;
   Unit u;
   u.P = GEN ? p.qpack : 1;
   u.span = C::BM / u.P;
@@ -725,7 +762,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     if (q0 < 0 || q1 < q0 || q1 > p.total_q || q1 - q0 > p.max_seqlen_q || k0 < 0 || k1 < k0 ||
         k1 > p.total_k || k1 - k0 > p.max_seqlen_k) {
       if (threadIdx.x == 0) atomicCAS(p.status, 0, (int)kDevBadSeqlens);
-      return;
+      active = false;
     }
     u.Lq = q1 - q0;
     u.Lk = k1 - k0;
@@ -742,9 +779,11 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     block = (int)(gridDim.x / p.num_splits) - 1 - (int)blockIdx.x / p.num_splits;
   }
   u.row0 = block * (KS ? 1 : NSUB) * u.span;
-  if (u.row0 >= u.Lq) return;  // uniform across the CTA
+  if (u.row0 >= u.Lq) active = false;
   u.delta = u.Lk - u.Lq;
-  if (KS) {  // one row block; sub-tile s takes the streamed tiles j = s mod 2
+  u.kt0 = u.n_tot = u.f0 = u.f1 = u.n0 = u.n1 = 0;
+  if (!active) {
+  } else if (KS) {  // one row block; sub-tile s takes the streamed tiles j = s mod 2
     const int2 r = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN);
     u.kt0 = r.x;
     u.n_tot = r.y > r.x ? r.y - r.x : 0;
@@ -768,41 +807,16 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     u.f1 = a1 ? r1.x - u.kt0 : 0;
     u.n1 = a1 ? r1.y - r1.x : 0;
   }
-  const int warp = threadIdx.x >> 5;
-  const bool producer = warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0;
-
-  if (producer) {
-    mbar_init(&sb.q_full, 1);
-#pragma unroll
-    for (int i = 0; i < C::K_STAGES; ++i) {
-      mbar_init(&sb.k_full[i], 1);
-      mbar_init(&sb.k_empty[i], 1);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sb.v_full[i], 1);
-      mbar_init(&sb.v_empty[i], 1);
-      mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.p_full[i], 128);
-      mbar_init(&sb.o_done[i], 1);
-    }
-    mbar_init(&sb.merge_ready, 128);
-    fence_mbar_init();
-    fence_proxy_async_smem();  // the initialised barriers, as the TMA (async proxy) will see them
-    // Q and the first key tile go out before the CTA's barrier (their
-    // slots are free and only this thread has touched the barriers yet).
-    producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1);
-  }
-  if (warp == C::MMA_WARP) {
-    tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
-    tmem_relinquish();
-  }
+  // Q and the first key tile go out before the CTA's barrier: their slots
+  // are free and only this thread has touched the barriers yet.
+  if (producer && active) producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sb.tmem_base;
 
-  if (warp < 4 * NSUB) {
+  if (!active) {
+  } else if (warp < 4 * NSUB) {
     if constexpr (NSUB == 2) regs_grow<C::SOFTMAX_REGS>();
     softmax_role<D, NSUB, BF16, GEN, KS>(sb, tmem, p, u, warp >> 2);
   } else {

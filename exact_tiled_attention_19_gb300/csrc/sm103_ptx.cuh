@@ -120,6 +120,12 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch: let the next grid on the stream be
+// scheduled now, and wait until the grids this one depends on have completed
+// and their memory operations are visible (a no-op without such a grid).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Make this thread's ordinary shared-memory stores visible to the async
 // proxy (TMA and the tensor core read shared memory through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
