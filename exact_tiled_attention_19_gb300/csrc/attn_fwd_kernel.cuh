@@ -165,6 +165,7 @@ struct SmemBarriers {
   uint64_t p_full[2];            // per sub-tile: P_s(j) written and O_s corrected
   uint64_t o_done[2];            // per sub-tile: last PV_s has completed
   uint64_t merge_ready;          // key split: sub-tile 1's (m, l) and O are final (128 arrivals)
+  uint64_t fin;                  // after a wait that ran out: every MMA issued so far has completed
   float merge_m[128], merge_l[128];  // key split: sub-tile 1's running max and sum per row
   uint32_t tmem_base;
 };
@@ -209,7 +210,8 @@ __device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit&
 template <int D, int NSUB, bool KS>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, SmemBarriers& sb, uint8_t* smem,
-                                              const Unit u, int hn_swapped, int* status, int j_from, int j_to) {
+                                              const Unit u, int hn_swapped, int* status, int j_from, int j_to,
+                                              int& k_issued, int& v_issued) {
   using C = TileCfg<D, NSUB>;
   constexpr int NQ = KS ? 1 : NSUB;  // Q tiles: the key split's sub-tiles share their rows
   const bool swq = hn_swapped & 1, swk = (hn_swapped >> 1) & 1, swv = (hn_swapped >> 2) & 1;
@@ -234,6 +236,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_K + ks * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmK, &sb.k_full[ks],
                       c * C::SW_ELEMS, key0, u.hk, u.bcoord, swk);
+      k_issued = j + 1;
     }
     if (++ks == C::K_STAGES) {
       ks = 0;
@@ -247,8 +250,22 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
       for (int c = 0; c < C::NCHUNK; ++c)
         tma_load_tile(smem + C::OFF_V + vs * C::KV_BYTES + c * C::BN * C::SW_BYTES, tmV, &sb.v_full[vs],
                       c * C::SW_ELEMS, key0, u.hk, u.bcoord, swv);
+      v_issued = j + 1;
     }
   }
+}
+
+// Waits (bounded) until the last load issued into every ring slot has landed,
+// so that no copy writes shared memory after the CTA exits.  After a normal
+// run the consumers already saw these phases complete and every wait returns
+// at once; after a wait ran out the loads still in flight are waited for.
+template <int D, int NSUB>
+__device__ __forceinline__ void producer_settle(SmemBarriers& sb, int k_issued, int v_issued) {
+  using C = TileCfg<D, NSUB>;
+  mbar_wait(&sb.q_full, 0, nullptr);
+  for (int t = k_issued > C::K_STAGES ? k_issued - C::K_STAGES : 0; t < k_issued; ++t)
+    mbar_wait(&sb.k_full[t % C::K_STAGES], (t / C::K_STAGES) & 1, nullptr);
+  for (int t = v_issued > 2 ? v_issued - 2 : 0; t < v_issued; ++t) mbar_wait(&sb.v_full[t & 1], (t >> 1) & 1, nullptr);
 }
 
 // ----------------------------------------------------------------- MMA issuer
@@ -732,6 +749,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
       mbar_init(&sb.o_done[i], 1);
     }
     mbar_init(&sb.merge_ready, 128);
+    mbar_init(&sb.fin, 1);
     fence_mbar_init();
     fence_proxy_async_smem();  // the initialised barriers, as the TMA (async proxy) will see them
     tma_prefetch_desc(&tmQ);
@@ -809,7 +827,9 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   }
   // Q and the first key tile go out before the CTA's barrier: their slots
   // are free and only this thread has touched the barriers yet.
-  if (producer && active) producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1);
+  int k_issued = 0, v_issued = 0;  // key / value tiles the producer has issued
+  if (producer && active)
+    producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1, k_issued, v_issued);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -823,13 +843,23 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     if constexpr (NSUB == 2) regs_shrink<C::CTRL_REGS>();
     const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp == C::PRODUCER_WARP) {
-      if (lane0) producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 1, 1 << 30);
+      if (lane0) {
+        producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 1, 1 << 30, k_issued,
+                                   v_issued);
+        if (u.n_tot > 0) producer_settle<D, NSUB>(sb, k_issued, v_issued);
+      }
       __syncwarp();
     } else if (warp == C::MMA_WARP) {
       constexpr uint32_t ab = BF16 ? 1u : 0u;
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
-      if (lane0) mma_role<D, NSUB, GEN, KS>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+      if (lane0) {
+        mma_role<D, NSUB, GEN, KS>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+        // Every MMA this thread issued has completed before tensor memory is
+        // released (immediate after a normal run; bounded after a wait ran out).
+        mma_commit(&sb.fin);
+        mbar_wait(&sb.fin, 0, nullptr);
+      }
       __syncwarp();
     }
   }
