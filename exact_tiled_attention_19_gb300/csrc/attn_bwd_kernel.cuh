@@ -117,6 +117,7 @@ struct BwdBarriers {
   uint64_t kv_done;                  // last dK / dV product done
   uint64_t stage_free;               // the dQ staging box may be written (leader, once per box)
   uint64_t stage_full;               // the dQ staging box is written (128 arrivals per box)
+  uint64_t fin;                      // every MMA the CTA issued has completed
   uint32_t tmem_base;
 };
 
@@ -140,7 +141,7 @@ __device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, uint
 template <int D>
 __device__ __forceinline__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                              const CUtensorMap* tmDO, BwdBarriers& sb, uint8_t* smem,
-                                             const BwdUnit u, const BwdParams& p) {
+                                             const BwdUnit u, const BwdParams& p, int& q_issued, int& do_issued) {
   using C = BwdCfg<D>;
   const bool swq = p.hn_swapped & 1, swk = p.hn_swapped & 2, swv = p.hn_swapped & 4, swd = p.hn_swapped & 8;
   mbar_arrive_expect_tx(&sb.kv_full, 2 * C::TILE);
@@ -159,6 +160,7 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tmQ, const CUten
       tma_tile(smem + C::OFF_Q + slot * C::TILE + c * 128 * C::SW_BYTES, tmQ, &sb.q_full[slot], c * C::SW_ELEMS, q0,
                h, u.b, swq);
     bulk_load(smem + C::OFF_LSE + slot * 512, p.nlse2 + vec_row, 512, &sb.q_full[slot]);
+    q_issued = i + 1;
     if (i >= 2 && !mbar_wait(&sb.do_empty[slot], ((i >> 1) - 1) & 1, p.status)) return;
     mbar_arrive_expect_tx(&sb.do_full[slot], C::TILE + 512);
 #pragma unroll
@@ -166,7 +168,19 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tmQ, const CUten
       tma_tile(smem + C::OFF_DO + slot * C::TILE + c * 128 * C::SW_BYTES, tmDO, &sb.do_full[slot], c * C::SW_ELEMS,
                q0, h, u.b, swd);
     bulk_load(smem + C::OFF_NSD + slot * 512, p.nsd + vec_row, 512, &sb.do_full[slot]);
+    do_issued = i + 1;
   }
+}
+
+// Waits (bounded) until the key/value tiles and the last load issued into each
+// Q and dO stage have landed, so that no copy writes shared memory after the
+// CTA exits (immediate after a normal run, whose consumers saw these phases).
+template <int D>
+__device__ __forceinline__ void bwd_producer_settle(BwdBarriers& sb, int q_issued, int do_issued) {
+  mbar_wait(&sb.kv_full, 0, nullptr);
+  for (int t = q_issued > 2 ? q_issued - 2 : 0; t < q_issued; ++t) mbar_wait(&sb.q_full[t & 1], (t >> 1) & 1, nullptr);
+  for (int t = do_issued > 2 ? do_issued - 2 : 0; t < do_issued; ++t)
+    mbar_wait(&sb.do_full[t & 1], (t >> 1) & 1, nullptr);
 }
 
 template <int D>
@@ -507,6 +521,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&sb.kv_done, 1);
     mbar_init(&sb.stage_free, 1);
     mbar_init(&sb.stage_full, 128);
+    mbar_init(&sb.fin, 1);
     fence_mbar_init();
   }
   if (warp == C::PRODUCER_WARP && (threadIdx.x & 31) == 0) {
@@ -535,10 +550,20 @@ __global__ void __launch_bounds__(512, 1)
     if (u.steps > 0) {
       const bool lane0 = (threadIdx.x & 31) == 0;
       if (warp == C::PRODUCER_WARP) {
-        if (lane0) bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, sb, smem, u, p);
+        if (lane0) {
+          int q_issued = 0, do_issued = 0;
+          bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, sb, smem, u, p, q_issued, do_issued);
+          bwd_producer_settle<D>(sb, q_issued, do_issued);
+        }
         __syncwarp();
       } else if (warp == C::MMA_WARP) {
-        if (lane0) bwd_mma<D>(sb, smem, tmem, u, BF16 ? 1u : 0u, p.status);
+        if (lane0) {
+          bwd_mma<D>(sb, smem, tmem, u, BF16 ? 1u : 0u, p.status);
+          // Every MMA issued has completed before tensor memory is released
+          // (immediate after a normal run; bounded after a wait ran out).
+          mma_commit(&sb.fin);
+          mbar_wait(&sb.fin, 0, nullptr);
+        }
         __syncwarp();
       }
     }
