@@ -497,6 +497,23 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     }
     return;
   }
+  // A warp none of whose rows exists (all past the query length: a ragged
+  // last block) keeps the barrier protocol and nothing else.  It releases
+  // each score tile without writing P (the PV product then fills only rows
+  // that are never stored), hands sub-tile 0 an empty state under the key
+  // split, and skips the epilogue.
+  if (!__any_sync(FULL, valid)) {
+    for (int j = 0; j < n; ++j) {
+      if (!warp_wait(&sb.s_full[s], j & 1, p.status)) return;
+      mbar_arrive(&sb.p_full[s]);
+    }
+    if (KS && s == 1) {
+      sb.merge_m[t] = -INFINITY;
+      sb.merge_l[t] = 0.f;
+      mbar_arrive(&sb.merge_ready);
+    }
+    return;
+  }
   const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
   const uint32_t tS = tmem + C::TM_S + s * 128 + lane_off;
   const uint32_t tO = tmem + C::TM_O + s * 128 + lane_off;
