@@ -25,11 +25,12 @@ Sources (web pages, cited by title and section):
   * "Attention algorithms and data movement" (study.greatitself.com), lessons
     01 (merging normalised attention), 03 (differentiating the normalised
     row), 04 (packed causal eligibility, unequal lengths), 05 (GQA head
-    mapping) and 07 (local windows).
+    mapping) and 07 (local windows, global-token unions).
 
 Parity status: every function here is pinned by CPU tests in
-``tests/test_oracle.py``, ``tests/test_oracle_lengths.py`` and
-``tests/test_oracle_backward.py`` against closed forms, a hand-worked example, library
+``tests/test_oracle.py``, ``tests/test_oracle_lengths.py``,
+``tests/test_oracle_global.py`` and ``tests/test_oracle_backward.py`` against
+closed forms (interval inclusion-exclusion counts among them), a hand-worked example, library
 routines (PyTorch's CPU scaled_dot_product_attention and its float64
 autograd, SciPy's logsumexp), finite differences, invariants and brute
 force; none is "parity unpinned".

@@ -28,6 +28,15 @@ Causal: j <= c_i.  An optional window keeps keys with
 c_i - window_left <= j <= c_i + window_right (-1 = unbounded on that side);
 causal is window_right = 0.
 
+Global tokens (same page, lesson 07, "global-token unions"; the pages give only
+the lesson's title, the reading taken here is the usual one): the first
+num_global positions of a sequence are global tokens.  Every row may also read
+the global keys, and a global row (c_i < num_global) may read every key; both
+still obey the causal mask, neither obeys the window.  So
+E(i) = C(i) ∩ (W(i) ∪ {j < num_global} ∪ [every key if c_i < num_global]),
+with C(i) the causal set and W(i) the window: a union of sets, in which a key
+that is both global and inside the window counts once.
+
 Empty rows (same page, lesson 01, explicit empty-row contract): a row with no
 eligible key (e.g. c_i < 0 under the causal mask when Lq > Lk) gets O = 0 and
 lse = -inf.
@@ -50,26 +59,29 @@ def kv_head_of(h, group):
     return h // group
 
 
-def eligible_keys(pos_rows, L, causal, Lq=None, window_left=-1, window_right=-1):
+def eligible_keys(pos_rows, L, causal, Lq=None, window_left=-1, window_right=-1, num_global=0):
     """[R, L] boolean eligibility of L keys for query rows at positions
     pos_rows (in 0..Lq-1; Lq defaults to L).  The row sits at key position
     c = pos + L - Lq.  Causal: key j is eligible iff j <= c (the diagonal is
     included, "Logic review before implementation"); a window further keeps
-    c - window_left <= j <= c + window_right (negative = unbounded)."""
+    c - window_left <= j <= c + window_right (negative = unbounded).  With
+    num_global = G > 0 the global keys j < G, and every key for a global row
+    (c < G), are added to the window's keys, under the causal mask only."""
     Lq = L if Lq is None else Lq
     c = np.asarray(pos_rows, dtype=np.int64)[:, None] + (L - Lq)
     j = np.arange(L)[None, :]
-    ok = np.ones((len(pos_rows), L), dtype=bool)
-    if causal:
-        ok &= j <= c
+    causal_ok = (j <= c) if causal else np.ones((len(pos_rows), L), dtype=bool)
+    window_ok = np.ones((len(pos_rows), L), dtype=bool)
     if window_right >= 0:
-        ok &= j <= c + window_right
+        window_ok &= j <= c + window_right
     if window_left >= 0:
-        ok &= j >= c - window_left
-    return ok
+        window_ok &= j >= c - window_left
+    if num_global > 0:
+        window_ok = window_ok | (j < num_global) | (c < num_global)
+    return causal_ok & window_ok
 
 
-def _rows_attention(q_rows, pos_rows, k, v, causal, scale, Lq=None, window_left=-1, window_right=-1):
+def _rows_attention(q_rows, pos_rows, k, v, causal, scale, Lq=None, window_left=-1, window_right=-1, num_global=0):
     """O and lse for query rows ``q_rows`` [R, D] at logical positions
     ``pos_rows`` [R] (of Lq query rows, default Lq = L) against keys ``k``
     [L, D] / values ``v`` [L, D] at positions 0..L-1."""
@@ -82,7 +94,7 @@ def _rows_attention(q_rows, pos_rows, k, v, causal, scale, Lq=None, window_left=
     if R == 0 or L == 0:
         return o, lse
     s = scale * (q_rows @ k.T)  # [R, L]
-    eligible = eligible_keys(pos_rows, L, causal, Lq, window_left, window_right)
+    eligible = eligible_keys(pos_rows, L, causal, Lq, window_left, window_right, num_global)
     nonempty = eligible.any(axis=1)
     s_masked = np.where(eligible, s, -np.inf)
     m = np.max(s_masked, axis=1)
@@ -94,17 +106,17 @@ def _rows_attention(q_rows, pos_rows, k, v, causal, scale, Lq=None, window_left=
     return o, lse
 
 
-def attention_rows(q, k, v, rows, *, causal, scale, window_left=-1, window_right=-1):
+def attention_rows(q, k, v, rows, *, causal, scale, window_left=-1, window_right=-1, num_global=0):
     """Attention for selected query positions of one (batch, head).
 
     q: [Nq, D], k, v: [Nk, D]; rows: int indices into 0..Nq-1.
     Returns (O [len(rows), D], lse [len(rows)])."""
     rows = np.asarray(rows, dtype=np.int64)
     return _rows_attention(np.asarray(q, dtype=np.float64)[rows], rows, k, v, causal, scale, len(q),
-                           window_left, window_right)
+                           window_left, window_right, num_global)
 
 
-def attention_dense(q, k, v, *, causal, scale, window_left=-1, window_right=-1):
+def attention_dense(q, k, v, *, causal, scale, window_left=-1, window_right=-1, num_global=0):
     """Batched multi-head attention.
 
     q: [B, Hq, Nq, D]; k, v: [B, Hkv, Nk, D] with Hq % Hkv == 0.
@@ -125,11 +137,13 @@ def attention_dense(q, k, v, *, causal, scale, window_left=-1, window_right=-1):
             for r0 in range(0, N, _ROW_CHUNK):
                 rows = np.arange(r0, min(N, r0 + _ROW_CHUNK))
                 o[b, h, rows], lse[b, h, rows] = _rows_attention(
-                    q[b, h, rows], rows, k[b, hk], v[b, hk], causal, scale, N, window_left, window_right)
+                    q[b, h, rows], rows, k[b, hk], v[b, hk], causal, scale, N, window_left, window_right,
+                    num_global)
     return o, lse
 
 
-def attention_varlen(q, k, v, cu_seqlens, *, causal, scale, cu_seqlens_k=None, window_left=-1, window_right=-1):
+def attention_varlen(q, k, v, cu_seqlens, *, causal, scale, cu_seqlens_k=None, window_left=-1, window_right=-1,
+                     num_global=0):
     """Packed variable-length attention.
 
     q: [Tq, Hq, D]; k, v: [Tk, Hkv, D]; cu_seqlens: [S+1] non-decreasing
@@ -157,12 +171,12 @@ def attention_varlen(q, k, v, cu_seqlens, *, causal, scale, cu_seqlens_k=None, w
                 rows = np.arange(r0, min(t1 - t0, r0 + _ROW_CHUNK))
                 o[t0 + rows, h], lse[h, t0 + rows] = _rows_attention(
                     q[t0 + rows, h], rows, k[k0:k1, hk], v[k0:k1, hk], causal, scale, t1 - t0,
-                    window_left, window_right)
+                    window_left, window_right, num_global)
     return o, lse
 
 
 def attention_varlen_rows(q, k, v, cu_seqlens, seq, head, rows, *, causal, scale, group=1, cu_seqlens_k=None,
-                          window_left=-1, window_right=-1):
+                          window_left=-1, window_right=-1, num_global=0):
     """Attention for selected logical positions ``rows`` of sequence ``seq``
     and query head ``head`` of a packed batch (layout as in attention_varlen).
     Returns (O [len(rows), D], lse [len(rows)])."""
@@ -173,4 +187,5 @@ def attention_varlen_rows(q, k, v, cu_seqlens, seq, head, rows, *, causal, scale
     rows = np.asarray(rows, dtype=np.int64)
     hk = kv_head_of(head, group)
     return _rows_attention(np.asarray(q[t0 + rows, head], dtype=np.float64), rows,
-                           k[k0:k1, hk], v[k0:k1, hk], causal, scale, t1 - t0, window_left, window_right)
+                           k[k0:k1, hk], v[k0:k1, hk], causal, scale, t1 - t0, window_left, window_right,
+                           num_global)

@@ -104,6 +104,6 @@ def test_varlen_separate_key_offsets_match_per_sequence_dense():
 def test_mutation_top_left_alignment_is_caught(monkeypatch):
     orig = dense.eligible_keys
     monkeypatch.setattr(dense, "eligible_keys",
-                        lambda pos, L, causal, Lq=None, wl=-1, wr=-1: orig(pos, L, causal, L, wl, wr))
+                        lambda pos, L, causal, Lq=None, wl=-1, wr=-1, g=0: orig(pos, L, causal, L, wl, wr, g))
     with pytest.raises(AssertionError):
         test_decode_rows_equal_the_suffix_of_the_square_problem(7, 300)
