@@ -38,7 +38,8 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; µs/call (1 GPU)
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PER_CONFIG = ["n129_d32_f16_causal", "n512_d64_f16_causal", "n512_d64_f16_noncausal", "n512_d64_f16_causal_qx30",
               "b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd", "gqa_b2_h32x8_n8192_d128_bf16",
-              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384", "decode_b8_h32x8_k32768",
+              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384",
+              "global64_window4096_n16384", "decode_b8_h32x8_k32768",
               "bwd_b4_h16_n4096_d128_bf16", "bwd_gqa_b2_h32x8_n8192_d128_bf16"]
 
 
@@ -214,6 +215,10 @@ def device_inputs(w, device):
         dev["ws"] = torch.empty(max(binding.attn_bwd_workspace_size(w.B, w.Hq, w.N, w.D), 1), dtype=torch.uint8,
                                 device=device)
         torch.cuda.synchronize()
+    if w.num_global > 0:
+        from exact_tiled_attention_19_gb300 import binding
+        need = binding.attn_fwd_global_workspace_size(w.B, w.Hq, w.N, w.D)
+        dev["ws"] = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
     if w.splitkv:
         from exact_tiled_attention_19_gb300 import binding
         rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.Hkv, w.N, w.keys)
@@ -225,11 +230,12 @@ def device_inputs(w, device):
 
 
 def launches_per_call(w):
-    """Kernels one call launches: the split-KV path adds the merge launch,
-    the backward pass a launch before (row statistics) and after (dQ)."""
+    """Kernels one call launches: the split-KV and global-token paths add
+    the merge launch, the backward pass a launch before (row statistics) and
+    after (dQ)."""
     if w.backward:
         return 3
-    return 2 if w.splitkv and w.keys > 0 else 1
+    return 2 if (w.splitkv or w.num_global > 0) and w.keys > 0 else 1
 
 
 def make_call(w, dev, stream):
@@ -248,6 +254,11 @@ def make_call(w, dev, stream):
             binding.attention_backward(dev["q"], dev["k"], dev["v"], dev["o"], dev["lse"], dev["dout"],
                                        causal=w.causal, scale=w.scale, dq=dev["dq"], dk=dev["dk"], dv=dev["dv"],
                                        workspace=dev["ws"], stream=stream, **win)
+    elif w.num_global > 0:
+        def call():
+            binding.attention_global(dev["q"], dev["k"], dev["v"], num_global=w.num_global, causal=w.causal,
+                                     scale=w.scale, workspace=dev["ws"], out=dev["o"], lse=dev["lse"],
+                                     stream=stream, **win)
     elif w.splitkv:
         def call():
             binding.attention_splitkv(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale,
@@ -397,6 +408,8 @@ def head_flops(w):
 def run_oracle_problem(prob, w):
     import oracle
     win = dict(window_left=w.window_left, window_right=w.window_right)
+    if w.num_global > 0:
+        win["num_global"] = w.num_global
     if w.backward:
         q, k, v, do = (x[None, None] for x in prob)
         return oracle.attention_backward_dense(q, k, v, do, causal=w.causal, scale=w.scale, **win)
@@ -452,6 +465,8 @@ def workload_config(w, n_gpus):
         cfg["key_len"] = w.keys
     if w.window_left >= 0 or w.window_right >= 0:
         cfg["window"] = {"left": w.window_left, "right": w.window_right}
+    if w.num_global > 0:
+        cfg["global_tokens"] = w.num_global
     if not w.square:
         cfg["flops"] = "exact eligible (query, key) pairs x 4 x D per head"
     return cfg
@@ -484,7 +499,8 @@ def correctness_gate(w, inp, dev):
             worst = max(worst, float(np.max(np.abs(f64(lse[0, t0:t0 + L][rows]) - rl))))
     elif w.N * w.B * w.Hq <= 4096:
         ro, rl = oracle.attention_dense(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), causal=w.causal, scale=w.scale,
-                                        window_left=w.window_left, window_right=w.window_right)
+                                        window_left=w.window_left, window_right=w.window_right,
+                                        num_global=w.num_global)
         worst = max(float(np.max(np.abs(f64(o) - ro))), float(np.max(np.abs(f64(lse) - rl))))
     else:
         rows = np.array(sorted({0, 1, 127, 128, w.N // 2, w.N - 1}))
@@ -492,7 +508,7 @@ def correctness_gate(w, inp, dev):
             hk = h // (w.Hq // w.Hkv)
             ro, rl = oracle.attention_rows(f64(inp["q"][b, h]), f64(inp["k"][b, hk]), f64(inp["v"][b, hk]), rows,
                                            causal=w.causal, scale=w.scale, window_left=w.window_left,
-                                           window_right=w.window_right)
+                                           window_right=w.window_right, num_global=w.num_global)
             worst = max(worst, float(np.max(np.abs(f64(o[b, h][rows]) - ro))),
                         float(np.max(np.abs(f64(lse[b, h][rows]) - rl))))
     return worst <= tol, worst

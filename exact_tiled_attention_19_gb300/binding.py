@@ -3,6 +3,7 @@
 The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_size``,
 ``attn_fwd_splitkv``, ``attn_fwd_splitkv_noalloc``,
 ``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
+``attn_fwd_global``, ``attn_fwd_global_workspace_size``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
 ``etattn_read_device_status`` and ``etattn_version`` have the C names and
@@ -84,6 +85,11 @@ def load_library(path: str | None = None):
         lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv_plan.argtypes = [_int] * 5 + [ctypes.POINTER(_int)]
         lib.attn_fwd_splitkv_plan.restype = _int
+        lib.attn_fwd_global.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 4 + [ctypes.c_float, _vp,
+                                        ctypes.c_size_t, _vp])
+        lib.attn_fwd_global.restype = _int
+        lib.attn_fwd_global_workspace_size.argtypes = [_int] * 4
+        lib.attn_fwd_global_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                                         _int, _i64p, _int, ctypes.c_float, _vp]
         lib.attn_fwd_varlen.restype = _int
@@ -132,6 +138,19 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, cau
     return lib.attn_fwd_splitkv(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D,
                                 dtype, _strides_arg(strides), causal, window_left, window_right, scale, num_splits,
                                 workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_global(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right,
+                    num_global, scale, workspace, workspace_bytes, stream):
+    """C ``attn_fwd_global``: pointers as ints (0 for NULL), ``strides`` 16 ints."""
+    lib = load_library()
+    return lib.attn_fwd_global(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D, dtype,
+                               _strides_arg(strides), causal, window_left, window_right, num_global, scale,
+                               workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_global_workspace_size(B, Hq, Nq, D) -> int:
+    return load_library().attn_fwd_global_workspace_size(B, Hq, Nq, D)
 
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left,
@@ -321,6 +340,38 @@ def attention_splitkv(q, k, v, *, causal: bool = True, scale: float | None = Non
                               int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != 0:
         raise EtattnError(rc, "attn_fwd_splitkv")
+    return out, lse
+
+
+def attention_global(q, k, v, *, num_global: int, causal: bool = True, scale: float | None = None,
+                     window_left: int = -1, window_right: int = -1, workspace=None, out=None, lse=None,
+                     return_lse: bool = True, stream=None):
+    """``attention`` with ``num_global`` global tokens beside the window (the
+    first positions read and are read by every row, under the causal mask).
+    ``workspace`` is a CUDA uint8 tensor of at least
+    ``attn_fwd_global_workspace_size`` bytes (allocated here when None)."""
+    import torch
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        need = attn_fwd_global_workspace_size(B, Hq, Nq, D)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
+        if lse is None and return_lse:
+            lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+        strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
+        ws_ptr = workspace.data_ptr() if workspace is not None else 0
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = attn_fwd_global(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr() if lse is not None else 0, B, Hq, Hkv, Nq, Nk, D, _dtype_code(q), strides,
+                             1 if causal else 0, int(window_left), int(window_right), int(num_global), float(scale),
+                             ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise EtattnError(rc, "attn_fwd_global")
     return out, lse
 
 

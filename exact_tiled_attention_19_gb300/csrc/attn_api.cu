@@ -356,13 +356,14 @@ int window_right_of(int wr, int causal) {
 // Validates every argument; launches only when do_launch is set.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
              int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
-             float scale, void* stream, bool do_launch, const SplitArgs* split = nullptr) {
+             float scale, void* stream, bool do_launch, const SplitArgs* split = nullptr, int num_global = 0) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
   if (Nq > kMaxTokens || Nk > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
+  if (num_global < 0 || (num_global > 0 && (split == nullptr || split->num_splits != 2))) return ETATTN_ERR_BAD_SHAPE;
   if (B == 0 || Hq == 0 || Nq == 0) return ETATTN_OK;  // empty output: nothing to do
   const bool has_keys = Nk > 0;
   if (!q || !o || (has_keys && (!k || !v))) return ETATTN_ERR_NULL_PTR;
@@ -448,6 +449,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   p.qpack = qpack;
+  // Global tokens: slice 1 of the split launch holds the global keys, slice 0
+  // the rest of each row's keys (the kernel's per-row key ranges).
+  p.num_global = splitting ? std::min(num_global, kMaxTokens) : 0;
+  p.win_right_causal = causal ? 0 : kUnboundedWindow;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (splitting) {
     const int key_tiles = (Nk + 127) / 128;
@@ -784,6 +789,26 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
   const SplitArgs sa{num_splits, workspace, workspace_bytes};
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
                   stream, true, &sa);
+}
+
+int attn_fwd_global(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                    int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left,
+                    int window_right, int num_global, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (num_global < 0) return ETATTN_ERR_BAD_SHAPE;
+  // The window already holds every key the causal mask allows: nothing to add.
+  const bool window_is_everything = window_left_of(window_left) == kUnboundedWindow &&
+                                    window_right_of(window_right, causal) == (causal ? 0 : kUnboundedWindow);
+  if (num_global == 0 || window_is_everything)
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                    stream, true);
+  const SplitArgs sa{2, workspace, workspace_bytes};
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
+                  stream, true, &sa, num_global);
+}
+
+size_t attn_fwd_global_workspace_size(int B, int Hq, int Nq, int D) {
+  return attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, 2);
 }
 
 // For callers that cannot allocate device memory at call time: a runtime

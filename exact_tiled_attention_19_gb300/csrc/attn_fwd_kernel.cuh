@@ -104,6 +104,9 @@ struct FwdParams {
   int64_t part_stride;           // rows per slice (the size of lse)
   int num_splits, split_tiles;   // key-tile slices; key tiles per slice
   int qpack;                     // query heads per 128-row sub-tile (1, or a power of two dividing group)
+  int num_global;                // global tokens (general build, two-slice split launch), else 0
+  int win_right_causal;          // 0 under the causal mask, else kUnboundedWindow: the bound a global
+                                 // token's connections keep
   float scale;                   // logit scale
   float scale_log2;              // scale * log2(e)
   int* status;                   // device status word
@@ -190,12 +193,42 @@ struct Unit {
   __device__ __forceinline__ bool reads(int s, int j) const { return (unsigned)(j - f(s)) < (unsigned)n(s); }
 };
 
+// Keys [lo, hi] (none when lo > hi) the row at key position c reads in this
+// launch.  Without global tokens: its window.  With G global tokens
+// ("Attention algorithms and data movement", lesson 07, global-token unions)
+// a row reads the global keys and its window, both under the causal mask
+// (limit h = c, or the last key), and a global row (c < G) reads every key
+// up to h.  That is two disjoint key intervals, computed as the two slices
+// of a split launch and merged: slice 1 holds [0, min(G - 1, h)], slice 0
+// the rest, [G, h] for a global row and the window clipped below at G
+// otherwise.  No key is counted in both.
+__device__ __forceinline__ int2 row_key_range(int c, const Unit& u, const FwdParams& p) {
+  int lo = max(0, c - p.win_left), hi = min(u.Lk - 1, c + p.win_right);
+  if (p.num_global > 0) {
+    const int G = p.num_global, h = min(u.Lk - 1, c + p.win_right_causal);
+    if (u.split == 1) {
+      lo = 0;
+      hi = min(G - 1, h);
+    } else if (c < G) {
+      lo = G;
+      hi = h;
+    } else {
+      lo = max(lo, G);
+    }
+  }
+  return make_int2(lo, hi);
+}
+
 // Key tiles [first, end) that some row of the query tokens [r0, r0 + span)
 // (clipped to the sequence) may read; {0, 0} when none may read any key.
+// A row's first key never decreases with its position; its last key does
+// not either, except that a global row may end past the first non-global
+// row's window: the first and last rows' ranges bound every row's.
 __device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit& u, const FwdParams& p, int bn) {
   if (r0 >= u.Lq) return make_int2(0, 0);
   const int c_first = r0 + u.delta, c_last = min(r0 + span - 1, u.Lq - 1) + u.delta;
-  const int lo = max(0, c_first - p.win_left), hi = min(u.Lk - 1, c_last + p.win_right);
+  const int2 a = row_key_range(c_first, u, p), b = row_key_range(c_last, u, p);
+  const int lo = min(a.x, b.x), hi = max(a.y, b.y);
   if (hi < lo) return make_int2(0, 0);
   return make_int2(lo / bn, hi / bn + 1);
 }
@@ -523,8 +556,15 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   // tile: lim_lo <= i <= lim_hi.  Both move down by one tile per step.
   const int c_row = row_pos + u.delta;
   const int kb0 = (u.kt0 + u.f(s)) * C::BN;
-  int lim_hi = min(u.Lk - 1, c_row + p.win_right) - kb0;
-  int lim_lo = max(0, c_row - p.win_left) - kb0;
+  int lim_hi, lim_lo;
+  if constexpr (GEN) {
+    const int2 kr = row_key_range(c_row, u, p);
+    lim_hi = kr.y - kb0;
+    lim_lo = kr.x - kb0;
+  } else {
+    lim_hi = min(u.Lk - 1, c_row + p.win_right) - kb0;
+    lim_lo = max(0, c_row - p.win_left) - kb0;
+  }
   float m_run = -INFINITY;  // running maximum of the raw scores (scale > 0)
   float l_run = 0.f;        // sum of exp2(c2 * (s - m_run)) over the keys seen
 
@@ -829,7 +869,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   } else {
     int2 r0 = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN);
     int2 r1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + u.span, u.span, u, p, C::BN) : make_int2(0, 0);
-    if (GEN && p.part_o != nullptr) {  // keep this slice's key tiles
+    if (GEN && p.part_o != nullptr && p.num_global == 0) {  // keep this slice's key tiles
       const int lo = u.split * p.split_tiles, hi = lo + p.split_tiles;
       r0 = make_int2(max(r0.x, lo), min(r0.y, hi));
       r1 = make_int2(max(r1.x, lo), min(r1.y, hi));

@@ -52,6 +52,7 @@ class Workload:
     seqlens_k: tuple = field(default_factory=tuple)  # packed key lengths; empty = seqlens
     window_left: int = -1         # local window (keys before the row's key position); -1 = none
     window_right: int = -1
+    num_global: int = 0           # global tokens beside the window (the first positions of each sequence)
     splitkv: bool = False         # run through the split-KV entry point (few queries, many keys)
     backward: bool = False        # the backward pass (dQ, dK, dV for a seeded upstream gradient)
 
@@ -81,7 +82,8 @@ class Workload:
     @property
     def square(self) -> bool:
         """Equal query and key lengths and no window."""
-        return all(lq == lk for lq, lk in self.lengths()) and self.window_left < 0 and self.window_right < 0
+        return (all(lq == lk for lq, lk in self.lengths()) and self.window_left < 0 and self.window_right < 0
+                and self.num_global == 0)
 
     def flops_convention(self) -> float:
         """4 * N^2 * D per (sequence, query head), halved when causal.  For
@@ -100,7 +102,10 @@ class Workload:
     def eligible_pairs(self) -> int:
         """(query row, key) pairs that enter the softmax, per query head,
         summed over sequences.  Query row r of Lq sits at key position
-        r + Lk - Lq; the causal mask and a window bound the keys it reads."""
+        r + Lk - Lq; the causal mask and a window bound the keys it reads.
+        With G global tokens a row also reads the keys below G and a global
+        row (position < G) every key, under the causal mask: the union is
+        counted by inclusion-exclusion, each pair once."""
         total = 0
         for lq, lk in self.lengths():
             if lq == 0 or lk == 0:
@@ -114,7 +119,15 @@ class Workload:
             lo = np.zeros(lq, dtype=np.int64)
             if self.window_left >= 0:
                 lo = np.maximum(lo, c - self.window_left)
-            total += int(np.maximum(hi - lo + 1, 0).sum())
+            n = np.maximum(hi - lo + 1, 0)
+            G = self.num_global
+            if G > 0:
+                hc = np.minimum(c, lk - 1) if self.causal else np.full(lq, lk - 1, dtype=np.int64)
+                bhi = np.minimum(G - 1, hc)                     # global keys [0, bhi]
+                n_b = np.maximum(bhi + 1, 0)
+                n_both = np.maximum(np.minimum(hi, bhi) - lo + 1, 0)
+                n = np.where(c < G, np.maximum(hc + 1, 0), n + n_b - n_both)
+            total += int(n.sum())
         return total
 
     def flops_exact(self) -> float:
@@ -165,6 +178,8 @@ WORKLOADS = dict([
            "causal), D=128, BF16", 2, 32, 8, 2048, 128, BF16, True, Nk=16384),
     _named("window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys (diagonal included), D=128, "
            "BF16", 2, 16, 16, 16384, 128, BF16, True, window_left=4095),
+    _named("global64_window4096_n16384", "B=2, H=16, N=16384, causal local window of 4096 keys plus 64 global "
+           "tokens, D=128, BF16", 2, 16, 16, 16384, 128, BF16, True, window_left=4095, num_global=64),
     # The backward pass of two forward workloads.
     _named("bwd_b4_h16_n4096_d128_bf16", "backward: B=4, H=16, N=4096, D=128, BF16, causal, [B,H,N,D]", 4, 16, 16,
            4096, 128, BF16, True, backward=True),

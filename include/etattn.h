@@ -168,6 +168,35 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
  * invalid sizes): num_splits * B*Hq*Nq * (4*D + 4) plus alignment padding. */
 size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_splits);
 
+/*
+ * attn_fwd_global: attn_fwd_ex plus num_global global tokens
+ * ("Attention algorithms and data movement", lesson 07, global-token
+ * unions).  The first num_global key positions are global: every row may
+ * also read the global keys j < num_global, and a global row (key position
+ * c < num_global) may read every key; both still obey the causal mask and
+ * ignore the window.  Row i's eligible keys are the union of its window and
+ * those connections, each key counted once.  The call runs one launch of two
+ * key slices (the global keys; the rest) and the split-KV merge launch, so
+ * the result equals the dense definition up to rounding order.
+ *
+ *   q, k, v, o, lse, strides, causal, windows, scale: as for attn_fwd_ex.
+ *   num_global: >= 0.  With 0, or when the window already holds every key
+ *           the causal mask allows (no left bound, and causal or no right
+ *           bound), the call is attn_fwd_ex and the workspace is not used.
+ *   workspace: as for attn_fwd_splitkv with num_splits = 2, at least
+ *           attn_fwd_global_workspace_size(B, Hq, Nq, D) bytes.
+ * Returns the codes of attn_fwd_splitkv; num_global < 0 is
+ * ETATTN_ERR_BAD_SHAPE.
+ */
+int attn_fwd_global(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                    int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left,
+                    int window_right, int num_global, float scale, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* Bytes of workspace attn_fwd_global needs: attn_fwd_splitkv_workspace_size
+ * with two slices (0 for invalid sizes). */
+size_t attn_fwd_global_workspace_size(int B, int Hq, int Nq, int D);
+
 /* A split count for attn_fwd_splitkv on the current device: enough CTAs for
  * about four per SM when the query tiles alone do not fill the GPU, each
  * slice at least four key tiles; 1 when splitting would not help.  (Fewer

@@ -64,14 +64,15 @@ def derived_bound(ro, v_absmax, keys, dtype):
     return u * v_absmax + u * np.abs(ro) + sub + 1e-5
 
 
-def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True, window_left=-1, window_right=-1):
+def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True, window_left=-1, window_right=-1,
+                 num_global=0):
     """Compare every output element with the dense oracle.  The stated bounds
     (max|dO| <= 2e-3 FP16 / 1e-2 BF16, max|d lse| <= 1e-3) must hold; for
     shapes outside the five specified workloads (derived_ok) an O element may
     instead meet the arithmetic bound of derived_bound.  Rows with no
     eligible key must be exact: O = 0 and lse = -inf."""
     q64, k64, v64 = to64(inputs["q"]), to64(inputs["k"]), to64(inputs["v"])
-    win = dict(window_left=window_left, window_right=window_right)
+    win = dict(window_left=window_left, window_right=window_right, num_global=num_global)
     if "cu_seqlens" in inputs:
         cu = inputs["cu_seqlens"].numpy()
         cuk = inputs["cu_seqlens_k"].numpy() if "cu_seqlens_k" in inputs else cu
@@ -117,18 +118,21 @@ def sample_rows(N, rng, extra=8):
     return sorted(r for r in base if 0 <= r < N)
 
 
-def compare_sampled_batched(inputs, o, lse, causal, scale, dtype, heads, rng, window_left=-1, window_right=-1):
+def compare_sampled_batched(inputs, o, lse, causal, scale, dtype, heads, rng, window_left=-1, window_right=-1,
+                            num_global=0, rows=None):
     """Compare sampled rows of selected (batch, head) pairs with the oracle
     computed row by row."""
     q, k, v = inputs["q"], inputs["k"], inputs["v"]
     Hq, Hkv, N = q.shape[1], k.shape[1], q.shape[2]
     group = Hq // Hkv
     worst_o = worst_l = 0.0
+    pick = rows
     for b, h in heads:
-        rows = sample_rows(N, rng)
+        rows = sample_rows(N, rng) if pick is None else pick
         hk = h // group
         ro, rl = oracle.attention_rows(to64(q[b, h]), to64(k[b, hk]), to64(v[b, hk]), rows, causal=causal,
-                                       scale=scale, window_left=window_left, window_right=window_right)
+                                       scale=scale, window_left=window_left, window_right=window_right,
+                                       num_global=num_global)
         go = to64(o[b, h][rows])
         gl = to64(lse[b, h][rows])
         worst_o = max(worst_o, float(np.max(np.abs(go - ro))))

@@ -283,6 +283,38 @@ def test_splitkv_valid_calls_need_a_device():
     assert rc == want and (rc != 0 or n >= 1)
 
 
+def global_call(num_global=8, wl=32, wr=-1, ws=0x70000000, ws_bytes=1 << 30, **kw):
+    a = good_args(**kw)
+    Nk = kw.get("Nk", a["N"])
+    st = (contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]) + contiguous_strides(a["B"], a["Hkv"], Nk, a["D"]) * 2
+          + contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]))
+    return B.attn_fwd_global(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], Nk, a["D"],
+                             a["dtype"], st, a["causal"], wl, wr, num_global, a["scale"], ws, ws_bytes, a["stream"])
+
+
+def test_global_workspace_is_two_slices():
+    assert B.attn_fwd_global_workspace_size(2, 8, 3, 128) == B.attn_fwd_splitkv_workspace_size(2, 8, 3, 128, 2)
+    assert B.attn_fwd_global_workspace_size(2, 8, 3, 96) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_global=-1), 3),
+    (dict(ws=0), 1), (dict(ws=0x70000010), 6), (dict(ws_bytes=1000), 3),
+    (dict(ws=Q), 7), (dict(Hkv=3), 4), (dict(N=-1), 3),
+])
+def test_global_invalid_arguments_rejected(kw, code):
+    assert global_call(**kw) == code
+
+
+def test_global_valid_calls_need_a_device_and_shortcuts_need_no_workspace():
+    import torch
+    want = 12 if not torch.cuda.is_available() else 0
+    assert global_call() == want
+    assert global_call(num_global=0, ws=0, ws_bytes=0) == want        # plain windowed call
+    assert global_call(wl=-1, ws=0, ws_bytes=0) == want               # causal, no left bound: the window is all
+    assert global_call(N=0) == 0                                       # no queries: no-op
+
+
 def noalloc_call(num_splits=4, **kw):
     a = good_args(**kw)
     Nk = kw.get("Nk", a["N"])
