@@ -4,6 +4,8 @@ The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_
 ``attn_fwd_splitkv``, ``attn_fwd_splitkv_noalloc``,
 ``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
 ``attn_fwd_global``, ``attn_fwd_global_workspace_size``,
+``attn_fwd_varlen_splitkv``, ``attn_fwd_varlen_splitkv_workspace_size``,
+``attn_fwd_varlen_global``, ``attn_fwd_varlen_global_workspace_size``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
 ``etattn_read_device_status`` and ``etattn_version`` have the C names and
@@ -70,6 +72,16 @@ def load_library(path: str | None = None):
         lib.attn_fwd_ex.restype = _int
         lib.attn_fwd_varlen_ex.argtypes = [_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 3 + [ctypes.c_float, _vp]
         lib.attn_fwd_varlen_ex.restype = _int
+        lib.attn_fwd_varlen_splitkv.argtypes = ([_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 3 +
+                                                [ctypes.c_float, _int, _vp, ctypes.c_size_t, _vp])
+        lib.attn_fwd_varlen_splitkv.restype = _int
+        lib.attn_fwd_varlen_splitkv_workspace_size.argtypes = [_int] * 4
+        lib.attn_fwd_varlen_splitkv_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_varlen_global.argtypes = ([_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 4 +
+                                               [ctypes.c_float, _vp, ctypes.c_size_t, _vp])
+        lib.attn_fwd_varlen_global.restype = _int
+        lib.attn_fwd_varlen_global_workspace_size.argtypes = [_int] * 3
+        lib.attn_fwd_varlen_global_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _int, _vp,
                                          ctypes.c_size_t, _vp])
         lib.attn_fwd_splitkv.restype = _int
@@ -412,10 +424,43 @@ def attention_backward(q, k, v, o, lse, dout, *, causal: bool = True, scale: flo
     return dq, dk, dv
 
 
+def attn_fwd_varlen_splitkv(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host,
+                            num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal,
+                            window_left, window_right, scale, num_splits, workspace, workspace_bytes, stream):
+    """C ``attn_fwd_varlen_splitkv``: pointers as ints; ``strides`` 12 ints."""
+    lib = load_library()
+    return lib.attn_fwd_varlen_splitkv(q or None, k or None, v or None, o or None, lse or None, cu_seqlens_q or None,
+                                       cu_seqlens_k or None, cu_seqlens_q_host or None, cu_seqlens_k_host or None,
+                                       num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype,
+                                       _strides_arg(strides), causal, window_left, window_right, scale, num_splits,
+                                       workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, num_splits) -> int:
+    return load_library().attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, num_splits)
+
+
+def attn_fwd_varlen_global(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host,
+                           num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal,
+                           window_left, window_right, num_global, scale, workspace, workspace_bytes, stream):
+    """C ``attn_fwd_varlen_global``: pointers as ints; ``strides`` 12 ints."""
+    lib = load_library()
+    return lib.attn_fwd_varlen_global(q or None, k or None, v or None, o or None, lse or None, cu_seqlens_q or None,
+                                      cu_seqlens_k or None, cu_seqlens_q_host or None, cu_seqlens_k_host or None,
+                                      num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype,
+                                      _strides_arg(strides), causal, window_left, window_right, num_global, scale,
+                                      workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_varlen_global_workspace_size(total_q, Hq, D) -> int:
+    return load_library().attn_fwd_varlen_global_workspace_size(total_q, Hq, D)
+
+
 def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = True, scale: float | None = None,
                      cu_seqlens_k=None, max_seqlen_k: int | None = None, window_left: int = -1,
                      window_right: int = -1, cu_seqlens_host=None, cu_seqlens_k_host=None, out=None, lse=None,
-                     return_lse: bool = True, stream=None):
+                     return_lse: bool = True, stream=None, num_splits: int = 1, num_global: int = 0,
+                     workspace=None):
     """Packed variable-length attention on CUDA tensors.
 
     q: [T, Hq, D]; k, v: [Tk, Hkv, D]; cu_seqlens: int32 CUDA tensor [S+1]
@@ -424,7 +469,10 @@ def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = Tru
     ``cu_seqlens_host`` / ``cu_seqlens_k_host`` (optional int32 CPU tensors)
     are validated before launch.  Returns (o [T, Hq, D], lse [Hq, T] FP32 or
     None).  Self-attention without a window goes through
-    ``attn_fwd_varlen``, the rest through ``attn_fwd_varlen_ex``."""
+    ``attn_fwd_varlen``, the rest through ``attn_fwd_varlen_ex``; with
+    ``num_splits`` > 1 through ``attn_fwd_varlen_splitkv`` and with
+    ``num_global`` > 0 through ``attn_fwd_varlen_global`` (``workspace``: a
+    CUDA uint8 tensor of their workspace size, allocated here when None)."""
     import torch
     T, Hq, D = q.shape
     Tk, Hkv = k.shape[0], k.shape[1]
@@ -449,9 +497,32 @@ def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = Tru
     cu_k_host, host_k_ptr = host_addr(cu_seqlens_k_host)
     strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
     lse_ptr = lse.data_ptr() if lse is not None else 0
-    plain = cu_seqlens_k is None and cu_k_host is None and window_left < 0 and window_right < 0
+    plain = (cu_seqlens_k is None and cu_k_host is None and window_left < 0 and window_right < 0 and num_splits <= 1
+             and num_global <= 0)
     with torch.cuda.device(q.device):
-        if plain:
+        if num_global > 0 or num_splits > 1:
+            cu_k = cu_seqlens if cu_seqlens_k is None else cu_seqlens_k
+            if cu_seqlens_k is None:
+                host_k_ptr = host_ptr
+            mk = int(max_seqlen if max_seqlen_k is None else max_seqlen_k)
+            need = (attn_fwd_varlen_global_workspace_size(T, Hq, D) if num_global > 0
+                    else attn_fwd_varlen_splitkv_workspace_size(T, Hq, D, int(num_splits)))
+            if workspace is None and need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            ws_ptr = workspace.data_ptr() if workspace is not None else 0
+            ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+            common = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, cu_seqlens.data_ptr(),
+                      cu_k.data_ptr(), host_ptr, host_k_ptr, S, int(max_seqlen), mk, T, Tk, Hq, Hkv, D,
+                      _dtype_code(q), strides, 1 if causal else 0, int(window_left), int(window_right))
+            if num_global > 0:
+                rc = attn_fwd_varlen_global(*common, int(num_global), float(scale), ws_ptr, ws_bytes,
+                                            _stream_handle(stream))
+                name = "attn_fwd_varlen_global"
+            else:
+                rc = attn_fwd_varlen_splitkv(*common, float(scale), int(num_splits), ws_ptr, ws_bytes,
+                                             _stream_handle(stream))
+                name = "attn_fwd_varlen_splitkv"
+        elif plain:
             rc = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
                                  cu_seqlens.data_ptr(), host_ptr, S, int(max_seqlen), T, Hq, Hkv, D, _dtype_code(q),
                                  strides, 1 if causal else 0, float(scale), _stream_handle(stream))
@@ -466,5 +537,7 @@ def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = Tru
                                     int(window_left), int(window_right), float(scale), _stream_handle(stream))
     del cu_host, cu_k_host
     if rc != 0:
-        raise EtattnError(rc, "attn_fwd_varlen" if plain else "attn_fwd_varlen_ex")
+        if num_global <= 0 and num_splits <= 1:
+            name = "attn_fwd_varlen" if plain else "attn_fwd_varlen_ex"
+        raise EtattnError(rc, name)
     return out, lse

@@ -676,7 +676,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
                 const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_k_host,
                 int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int D,
                 int dtype, const int64_t* strides, int causal, int window_left, int window_right, float scale,
-                void* stream, bool do_launch) {
+                void* stream, bool do_launch, const SplitArgs* split = nullptr, int num_global = 0) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq < 0 ||
       !head_dim_ok(D))
@@ -686,6 +686,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
+  if (num_global < 0 || (num_global > 0 && (split == nullptr || split->num_splits != 2))) return ETATTN_ERR_BAD_SHAPE;
+  if (split != nullptr && (split->num_splits < 1 || split->num_splits > kMaxSplits)) return ETATTN_ERR_BAD_SHAPE;
   if (cu_seqlens_q_host && !seqlens_ok(cu_seqlens_q_host, num_seqs, total_q, max_seqlen_q))
     return ETATTN_ERR_BAD_SEQLENS;
   if (cu_seqlens_k_host && !seqlens_ok(cu_seqlens_k_host, num_seqs, total_k, max_seqlen_k))
@@ -711,6 +713,21 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   for (const View* t : {&vq, &vk, &vv})
     if (overlaps(vo, 2, *t, 2) || (lse && overlaps(vl, 4, *t, 2))) return ETATTN_ERR_ALIAS;
   if (lse && overlaps(vl, 4, vo, 2)) return ETATTN_ERR_ALIAS;
+  // Split-KV: as in fwd_impl, one partial state per (slice, query head,
+  // token) row, at the row's lse index h * T + t.
+  const int64_t rows = (int64_t)Hq * T;
+  const bool splitting = split != nullptr && split->num_splits > 1 && has_keys;
+  if (splitting) {
+    const size_t need = splitkv_bytes(rows, D, split->num_splits);
+    if (need == 0) return ETATTN_ERR_BAD_SHAPE;
+    if (split->workspace == nullptr) return ETATTN_ERR_NULL_PTR;
+    if (reinterpret_cast<uintptr_t>(split->workspace) % kWorkspaceAlign) return ETATTN_ERR_BAD_ALIGN;
+    if (split->workspace_bytes < need) return ETATTN_ERR_BAD_SHAPE;
+    const View vw{split->workspace, 1, {(int64_t)need, 0, 0, 0}, {1, 0, 0, 0}};
+    for (const View* t : {&vq, &vk, &vv, &vo})
+      if (overlaps(vw, 1, *t, 2)) return ETATTN_ERR_ALIAS;
+    if (lse && overlaps(vw, 1, vl, 4)) return ETATTN_ERR_ALIAS;
+  }
   if (!do_launch) return ETATTN_OK;
 
   int dev = 0;
@@ -720,7 +737,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
   // Shared query and key offsets mean equal lengths in every sequence (see
   // fwd_impl for why the right bound does not matter).
-  const bool general = cu_seqlens_k != cu_seqlens_q || window_left_of(window_left) != kUnboundedWindow;
+  const bool general =
+      cu_seqlens_k != cu_seqlens_q || window_left_of(window_left) != kUnboundedWindow || splitting;
   const int qpack = qpack_of(general, Hq / Hkv, max_seqlen_q);
 
   CUtensorMap mq, mk, mv;
@@ -759,10 +777,39 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   p.qpack = qpack;
+  p.num_global = splitting ? std::min(num_global, kMaxTokens) : 0;
+  p.win_right_causal = causal ? 0 : kUnboundedWindow;
+  const int64_t key_tiles = ((int64_t)max_seqlen_k + 127) / 128;
+  if (splitting) {
+    uint8_t* ws = static_cast<uint8_t*>(split->workspace);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.part_lse = reinterpret_cast<float*>(ws + splitkv_lse_offset(rows, D, split->num_splits));
+    p.part_stride = rows;
+    p.num_splits = split->num_splits;
+    p.split_tiles = (int)((key_tiles + split->num_splits - 1) / split->num_splits);
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)max_seqlen_q * qpack, (unsigned)(Hq / qpack),
-                         (unsigned)num_seqs, num_sms, general, static_cast<cudaStream_t>(stream),
-                         ((int64_t)max_seqlen_k + 127) / 128);
+                         (unsigned)num_seqs, num_sms, general, st, key_tiles);
   if (e != cudaSuccess) return fail_cuda(e);
+  if (splitting) {
+    CombineParams c{};
+    c.part_o = p.part_o;
+    c.part_lse = p.part_lse;
+    c.rows = rows;
+    c.num_splits = p.num_splits;
+    c.o = o;
+    c.lse = lse;
+    c.o_sb = 0;
+    c.o_sh = strides[10];
+    c.o_sn = strides[9];
+    c.Hq = Hq;
+    c.Nq = 0;
+    c.packed = 1;
+    c.total = T;
+    e = launch_combine(D, dtype == ETATTN_BF16, c, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   return ETATTN_OK;
 }
 
@@ -885,6 +932,46 @@ int attn_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, flo
   return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
                      max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
                      window_right, scale, stream, true);
+}
+
+int attn_fwd_varlen_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
+                            const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                            int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides,
+                            int causal, int window_left, int window_right, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  const SplitArgs sa{num_splits, workspace, workspace_bytes};
+  return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
+                     max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
+                     window_right, scale, stream, true, &sa);
+}
+
+size_t attn_fwd_varlen_splitkv_workspace_size(int total_q, int Hq, int D, int num_splits) {
+  if (total_q < 0 || Hq < 0 || !head_dim_ok(D) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_bytes((int64_t)total_q * Hq, D, num_splits);
+}
+
+int attn_fwd_varlen_global(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
+                           const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                           int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides,
+                           int causal, int window_left, int window_right, int num_global, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_global < 0) return ETATTN_ERR_BAD_SHAPE;
+  const bool window_is_everything = window_left_of(window_left) == kUnboundedWindow &&
+                                    window_right_of(window_right, causal) == (causal ? 0 : kUnboundedWindow);
+  if (num_global == 0 || window_is_everything)
+    return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
+                       max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
+                       window_right, scale, stream, true);
+  const SplitArgs sa{2, workspace, workspace_bytes};
+  return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
+                     max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
+                     window_right, scale, stream, true, &sa, num_global);
+}
+
+size_t attn_fwd_varlen_global_workspace_size(int total_q, int Hq, int D) {
+  return attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, 2);
 }
 
 int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,

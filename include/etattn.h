@@ -197,6 +197,47 @@ int attn_fwd_global(const void* q, const void* k, const void* v, void* o, float*
  * with two slices (0 for invalid sizes). */
 size_t attn_fwd_global_workspace_size(int B, int Hq, int Nq, int D);
 
+/*
+ * attn_fwd_varlen_splitkv: attn_fwd_varlen_ex with the keys of every
+ * sequence cut into num_splits slices (as attn_fwd_splitkv does for the
+ * batched layout), for packed batches of few query rows over long keys.
+ * Slice s of a sequence holds its key tiles s*m .. s*m + m - 1 with
+ * m = ceil(ceil(max_seqlen_k / 128) / num_splits).
+ *
+ *   arguments as for attn_fwd_varlen_ex, plus num_splits, workspace and
+ *   workspace_bytes as for attn_fwd_splitkv; the workspace holds
+ *   attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, num_splits) bytes
+ *   (one partial row per slice, query head and query token).
+ */
+int attn_fwd_varlen_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
+                            const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                            int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides,
+                            int causal, int window_left, int window_right, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_fwd_varlen_splitkv needs (0 when num_splits <= 1 or
+ * for invalid sizes): num_splits * total_q*Hq * (4*D + 4) plus padding. */
+size_t attn_fwd_varlen_splitkv_workspace_size(int total_q, int Hq, int D, int num_splits);
+
+/*
+ * attn_fwd_varlen_global: attn_fwd_varlen_ex plus num_global global tokens
+ * per sequence (the first num_global positions of each sequence), with the
+ * rule and the two-slice computation of attn_fwd_global.  The workspace
+ * holds attn_fwd_varlen_global_workspace_size(total_q, Hq, D) bytes; with
+ * num_global = 0, or a window that already holds every key the causal mask
+ * allows, the call is attn_fwd_varlen_ex and the workspace is not used.
+ */
+int attn_fwd_varlen_global(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
+                           const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
+                           int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides,
+                           int causal, int window_left, int window_right, int num_global, float scale,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_fwd_varlen_global needs (two slices). */
+size_t attn_fwd_varlen_global_workspace_size(int total_q, int Hq, int D);
+
 /* A split count for attn_fwd_splitkv on the current device: enough CTAs for
  * about four per SM when the query tiles alone do not fill the GPU, each
  * slice at least four key tiles; 1 when splitting would not help.  (Fewer

@@ -244,6 +244,51 @@ def test_varlen_ex_argument_errors():
     assert varlen_ex_call(num_seqs=0) == 0
 
 
+def varlen_split_call(kind="split", num_splits=4, num_global=8, ws=0x70000000, ws_bytes=1 << 30, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=LSE, cuq=0x60000000, cuk=0x60001000, num_seqs=3, mq=50, mk=80, Tq=100, Tk=150,
+             Hq=4, Hkv=2, D=128, dtype=1, causal=1, wl=32, wr=-1, scale=0.1, stream=0)
+    a.update(kw)
+    st = [a["Hq"] * a["D"], a["D"], 1, a["Hkv"] * a["D"], a["D"], 1, a["Hkv"] * a["D"], a["D"], 1,
+          a["Hq"] * a["D"], a["D"], 1]
+    common = (a["q"], a["k"], a["v"], a["o"], a["lse"], a["cuq"], a["cuk"], 0, 0, a["num_seqs"], a["mq"], a["mk"],
+              a["Tq"], a["Tk"], a["Hq"], a["Hkv"], a["D"], a["dtype"], st, a["causal"], a["wl"], a["wr"])
+    if kind == "split":
+        return B.attn_fwd_varlen_splitkv(*common, a["scale"], num_splits, ws, ws_bytes, a["stream"])
+    return B.attn_fwd_varlen_global(*common, num_global, a["scale"], ws, ws_bytes, a["stream"])
+
+
+def test_varlen_split_and_global_workspace_formulas():
+    rows = 100 * 4
+    o_bytes = 3 * rows * 128 * 4
+    padded = (o_bytes + 255) // 256 * 256
+    assert B.attn_fwd_varlen_splitkv_workspace_size(100, 4, 128, 3) == padded + 3 * rows * 4
+    assert B.attn_fwd_varlen_splitkv_workspace_size(100, 4, 128, 1) == 0
+    assert B.attn_fwd_varlen_global_workspace_size(100, 4, 128) == B.attn_fwd_varlen_splitkv_workspace_size(100, 4,
+                                                                                                            128, 2)
+
+
+@pytest.mark.parametrize("kind", ["split", "global"])
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), 1), (dict(ws=0x70000010), 6), (dict(ws_bytes=1000), 3), (dict(ws=Q), 7),
+    (dict(Hkv=3), 4), (dict(cuk=0), 1), (dict(mk=-1), 3),
+])
+def test_varlen_split_and_global_invalid_arguments_rejected(kind, kw, code):
+    assert varlen_split_call(kind, **kw) == code
+
+
+def test_varlen_split_and_global_special_values():
+    import torch
+    want = 12 if not torch.cuda.is_available() else 0
+    assert varlen_split_call("split", num_splits=0) == 3
+    assert varlen_split_call("split", num_splits=1025) == 3
+    assert varlen_split_call("global", num_global=-1) == 3
+    assert varlen_split_call("split") == want
+    assert varlen_split_call("global") == want
+    assert varlen_split_call("split", num_splits=1, ws=0, ws_bytes=0) == want   # one slice: no workspace
+    assert varlen_split_call("global", num_global=0, ws=0, ws_bytes=0) == want  # no global token: plain call
+    assert varlen_split_call("split", Tq=0) == 0
+
+
 def test_splitkv_workspace_size_formula():
     rows = 2 * 8 * 3
     o_bytes = 5 * rows * 128 * 4

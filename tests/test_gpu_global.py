@@ -118,3 +118,28 @@ def test_global_window_workload_sampled():
     compare_sampled_batched(inp_dev, o, lse, True, default_scale(w.D), w.dtype, [(0, 0), (0, w.Hq - 1)], rng,
                             window_left=w.window_left, window_right=w.window_right, num_global=w.num_global,
                             rows=rows)
+
+
+@pytest.mark.parametrize("causal,wl,wr", [(True, 48, 0), (False, 20, 30)])
+def test_varlen_global_tokens_are_per_sequence(causal, wl, wr):
+    """Packed batches: the first G positions of every sequence are global."""
+    inp = W.random_varlen([1, 0, 129, 700, 40, 333], 4, 2, 128, torch.bfloat16, seed=14)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    cu = inp["cu_seqlens"]
+    lens = (cu[1:] - cu[:-1]).tolist()
+    o, lse = binding.attention_varlen(q, k, v, cu.cuda(), max(lens), causal=causal, cu_seqlens_host=cu,
+                                      num_global=17, window_left=wl, window_right=wr)
+    torch.cuda.synchronize()
+    compare_full(inp, o, lse, causal, default_scale(128), torch.bfloat16, window_left=wl, window_right=wr,
+                 num_global=17)
+
+
+def test_varlen_global_with_separate_key_offsets():
+    inp = W.random_varlen([20, 5, 128], 8, 2, 64, torch.float16, seed=15, lengths_k=[400, 60, 128])
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    cu, cuk = inp["cu_seqlens"], inp["cu_seqlens_k"]
+    o, lse = binding.attention_varlen(q, k, v, cu.cuda(), 128, causal=True, cu_seqlens_host=cu,
+                                      cu_seqlens_k=cuk.cuda(), max_seqlen_k=400, cu_seqlens_k_host=cuk,
+                                      num_global=10, window_left=32)
+    torch.cuda.synchronize()
+    compare_full(inp, o, lse, True, default_scale(64), torch.float16, window_left=32, num_global=10)

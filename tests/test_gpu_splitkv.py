@@ -126,3 +126,43 @@ def test_named_decode_workload():
     rng = np.random.default_rng(3)
     heads = [(b, h) for b in (0, w.B - 1) for h in (0, 5, w.Hq - 1)]
     compare_sampled_batched(inp, o.cpu(), lse.cpu(), w.causal, w.scale, w.dtype, heads, rng)
+
+
+# ---------------------------------------------------------------- packed batches (attn_fwd_varlen_splitkv)
+
+def run_varlen_split(inp, causal, num_splits, window_left=-1, window_right=-1):
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    cu = inp["cu_seqlens"]
+    cuk = inp.get("cu_seqlens_k", cu)
+    lq, lk = (cu[1:] - cu[:-1]).tolist(), (cuk[1:] - cuk[:-1]).tolist()
+    kw = dict(cu_seqlens_k=cuk.cuda(), max_seqlen_k=max(lk), cu_seqlens_k_host=cuk) if "cu_seqlens_k" in inp else {}
+    o, lse = binding.attention_varlen(q, k, v, cu.cuda(), max(lq), causal=causal, cu_seqlens_host=cu,
+                                      num_splits=num_splits, window_left=window_left, window_right=window_right,
+                                      **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+@pytest.mark.parametrize("splits", [2, 5])
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_splitkv_self_attention_matches_oracle(splits, causal):
+    inp = W.random_varlen([1, 0, 129, 700, 33, 1500], 4, 2, 128, torch.bfloat16, seed=splits)
+    o, lse = run_varlen_split(inp, causal, splits)
+    compare_full(inp, o, lse, causal, default_scale(128), torch.bfloat16)
+
+
+@pytest.mark.parametrize("splits", [3, 8])
+def test_varlen_splitkv_decode_rows_over_long_keys(splits):
+    """A few query rows per sequence over long key histories (packed
+    decode): bottom-right causal, grouped-query heads packed per tile, a
+    sequence without keys and one without queries."""
+    inp = W.random_varlen([1, 4, 0, 2, 1], 16, 4, 128, torch.bfloat16, seed=10 + splits,
+                          lengths_k=[3000, 257, 900, 0, 1])
+    o, lse = run_varlen_split(inp, True, splits)
+    compare_full(inp, o, lse, True, default_scale(128), torch.bfloat16)
+
+
+def test_varlen_splitkv_with_window_equals_oracle():
+    inp = W.random_varlen([300, 1000, 64], 4, 4, 64, torch.float16, seed=21)
+    o, lse = run_varlen_split(inp, True, 4, window_left=200)
+    compare_full(inp, o, lse, True, default_scale(64), torch.float16, window_left=200)
