@@ -5,6 +5,7 @@ The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_
 ``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
 ``attn_fwd_global``, ``attn_fwd_global_workspace_size``,
 ``attn_fwd_varlen_splitkv``, ``attn_fwd_varlen_splitkv_workspace_size``,
+``attn_fwd_varlen_splitkv_plan``,
 ``attn_fwd_varlen_global``, ``attn_fwd_varlen_global_workspace_size``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
@@ -75,6 +76,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_varlen_splitkv.argtypes = ([_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 3 +
                                                 [ctypes.c_float, _int, _vp, ctypes.c_size_t, _vp])
         lib.attn_fwd_varlen_splitkv.restype = _int
+        lib.attn_fwd_varlen_splitkv_plan.argtypes = [_int] * 5 + [ctypes.POINTER(_int)]
+        lib.attn_fwd_varlen_splitkv_plan.restype = _int
         lib.attn_fwd_varlen_splitkv_workspace_size.argtypes = [_int] * 4
         lib.attn_fwd_varlen_splitkv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_varlen_global.argtypes = ([_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 4 +
@@ -434,6 +437,14 @@ def attn_fwd_varlen_splitkv(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seql
                                        num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype,
                                        _strides_arg(strides), causal, window_left, window_right, scale, num_splits,
                                        workspace or None, workspace_bytes, stream or None)
+
+
+def attn_fwd_varlen_splitkv_plan(num_seqs, Hq, Hkv, max_seqlen_q, max_seqlen_k):
+    """(status, num_splits) for the current device."""
+    out = _int(0)
+    rc = load_library().attn_fwd_varlen_splitkv_plan(num_seqs, Hq, Hkv, max_seqlen_q, max_seqlen_k,
+                                                      ctypes.byref(out))
+    return rc, out.value
 
 
 def attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, num_splits) -> int:

@@ -951,6 +951,13 @@ size_t attn_fwd_varlen_splitkv_workspace_size(int total_q, int Hq, int D, int nu
   return splitkv_bytes((int64_t)total_q * Hq, D, num_splits);
 }
 
+int attn_fwd_varlen_splitkv_plan(int num_seqs, int Hq, int Hkv, int max_seqlen_q, int max_seqlen_k,
+                                 int* num_splits) {
+  // The batched planner's wave model with every sequence as long as the
+  // longest: the grid has num_seqs sequences of max_seqlen_q query rows.
+  return attn_fwd_splitkv_plan(num_seqs, Hq, Hkv, max_seqlen_q, max_seqlen_k, num_splits);
+}
+
 int attn_fwd_varlen_global(const void* q, const void* k, const void* v, void* o, float* lse,
                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
                            const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,

@@ -220,6 +220,13 @@ int attn_fwd_varlen_splitkv(const void* q, const void* k, const void* v, void* o
  * for invalid sizes): num_splits * total_q*Hq * (4*D + 4) plus padding. */
 size_t attn_fwd_varlen_splitkv_workspace_size(int total_q, int Hq, int D, int num_splits);
 
+/* A split count for attn_fwd_varlen_splitkv: attn_fwd_splitkv_plan for a
+ * batch of num_seqs sequences of max_seqlen_q queries over max_seqlen_k keys
+ * (the launch's grid covers every sequence at the longest lengths).  Same
+ * return codes as attn_fwd_splitkv_plan. */
+int attn_fwd_varlen_splitkv_plan(int num_seqs, int Hq, int Hkv, int max_seqlen_q, int max_seqlen_k,
+                                 int* num_splits);
+
 /*
  * attn_fwd_varlen_global: attn_fwd_varlen_ex plus num_global global tokens
  * per sequence (the first num_global positions of each sequence), with the

@@ -287,6 +287,9 @@ def test_varlen_split_and_global_special_values():
     assert varlen_split_call("split", num_splits=1, ws=0, ws_bytes=0) == want   # one slice: no workspace
     assert varlen_split_call("global", num_global=0, ws=0, ws_bytes=0) == want  # no global token: plain call
     assert varlen_split_call("split", Tq=0) == 0
+    rc, n = B.attn_fwd_varlen_splitkv_plan(8, 32, 8, 1, 32768)
+    assert rc == want and (rc != 0 or n >= 1)
+    assert B.attn_fwd_varlen_splitkv_plan(8, 32, 3, 1, 32768)[0] == 4    # Hq % Hkv != 0
 
 
 def test_splitkv_workspace_size_formula():
