@@ -215,10 +215,6 @@ def device_inputs(w, device):
         dev["ws"] = torch.empty(max(binding.attn_bwd_workspace_size(w.B, w.Hq, w.N, w.D), 1), dtype=torch.uint8,
                                 device=device)
         torch.cuda.synchronize()
-    if w.num_global > 0:
-        from exact_tiled_attention_19_gb300 import binding
-        need = binding.attn_fwd_global_workspace_size(w.B, w.Hq, w.N, w.D)
-        dev["ws"] = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
     if w.splitkv:
         from exact_tiled_attention_19_gb300 import binding
         rc, n = binding.attn_fwd_splitkv_plan(w.B, w.Hq, w.Hkv, w.N, w.keys)
@@ -230,12 +226,11 @@ def device_inputs(w, device):
 
 
 def launches_per_call(w):
-    """Kernels one call launches: the split-KV and global-token paths add
-    the merge launch, the backward pass a launch before (row statistics) and
-    after (dQ)."""
+    """Kernels one call launches: the split-KV path adds the merge launch,
+    the backward pass a launch before (row statistics) and after (dQ)."""
     if w.backward:
         return 3
-    return 2 if (w.splitkv or w.num_global > 0) and w.keys > 0 else 1
+    return 2 if w.splitkv and w.keys > 0 else 1
 
 
 def make_call(w, dev, stream):
@@ -257,8 +252,7 @@ def make_call(w, dev, stream):
     elif w.num_global > 0:
         def call():
             binding.attention_global(dev["q"], dev["k"], dev["v"], num_global=w.num_global, causal=w.causal,
-                                     scale=w.scale, workspace=dev["ws"], out=dev["o"], lse=dev["lse"],
-                                     stream=stream, **win)
+                                     scale=w.scale, out=dev["o"], lse=dev["lse"], stream=stream, **win)
     elif w.splitkv:
         def call():
             binding.attention_splitkv(dev["q"], dev["k"], dev["v"], causal=w.causal, scale=w.scale,

@@ -3,10 +3,10 @@
 The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_size``,
 ``attn_fwd_splitkv``, ``attn_fwd_splitkv_noalloc``,
 ``attn_fwd_splitkv_workspace_size``, ``attn_fwd_splitkv_plan``,
-``attn_fwd_global``, ``attn_fwd_global_workspace_size``,
+``attn_fwd_global``,
 ``attn_fwd_varlen_splitkv``, ``attn_fwd_varlen_splitkv_workspace_size``,
 ``attn_fwd_varlen_splitkv_plan``,
-``attn_fwd_varlen_global``, ``attn_fwd_varlen_global_workspace_size``,
+``attn_fwd_varlen_global``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
 ``etattn_read_device_status`` and ``etattn_version`` have the C names and
@@ -80,11 +80,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_varlen_splitkv_plan.restype = _int
         lib.attn_fwd_varlen_splitkv_workspace_size.argtypes = [_int] * 4
         lib.attn_fwd_varlen_splitkv_workspace_size.restype = ctypes.c_size_t
-        lib.attn_fwd_varlen_global.argtypes = ([_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 4 +
-                                               [ctypes.c_float, _vp, ctypes.c_size_t, _vp])
+        lib.attn_fwd_varlen_global.argtypes = [_vp] * 9 + [_int] * 9 + [_i64p] + [_int] * 4 + [ctypes.c_float, _vp]
         lib.attn_fwd_varlen_global.restype = _int
-        lib.attn_fwd_varlen_global_workspace_size.argtypes = [_int] * 3
-        lib.attn_fwd_varlen_global_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 3 + [ctypes.c_float, _int, _vp,
                                          ctypes.c_size_t, _vp])
         lib.attn_fwd_splitkv.restype = _int
@@ -100,11 +97,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv_plan.argtypes = [_int] * 5 + [ctypes.POINTER(_int)]
         lib.attn_fwd_splitkv_plan.restype = _int
-        lib.attn_fwd_global.argtypes = ([_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 4 + [ctypes.c_float, _vp,
-                                        ctypes.c_size_t, _vp])
+        lib.attn_fwd_global.argtypes = [_vp] * 5 + [_int] * 7 + [_i64p] + [_int] * 4 + [ctypes.c_float, _vp]
         lib.attn_fwd_global.restype = _int
-        lib.attn_fwd_global_workspace_size.argtypes = [_int] * 4
-        lib.attn_fwd_global_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                                         _int, _i64p, _int, ctypes.c_float, _vp]
         lib.attn_fwd_varlen.restype = _int
@@ -156,16 +150,12 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, cau
 
 
 def attn_fwd_global(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right,
-                    num_global, scale, workspace, workspace_bytes, stream):
+                    num_global, scale, stream):
     """C ``attn_fwd_global``: pointers as ints (0 for NULL), ``strides`` 16 ints."""
     lib = load_library()
     return lib.attn_fwd_global(q or None, k or None, v or None, o or None, lse or None, B, Hq, Hkv, Nq, Nk, D, dtype,
                                _strides_arg(strides), causal, window_left, window_right, num_global, scale,
-                               workspace or None, workspace_bytes, stream or None)
-
-
-def attn_fwd_global_workspace_size(B, Hq, Nq, D) -> int:
-    return load_library().attn_fwd_global_workspace_size(B, Hq, Nq, D)
+                               stream or None)
 
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left,
@@ -359,32 +349,25 @@ def attention_splitkv(q, k, v, *, causal: bool = True, scale: float | None = Non
 
 
 def attention_global(q, k, v, *, num_global: int, causal: bool = True, scale: float | None = None,
-                     window_left: int = -1, window_right: int = -1, workspace=None, out=None, lse=None,
-                     return_lse: bool = True, stream=None):
+                     window_left: int = -1, window_right: int = -1, out=None, lse=None, return_lse: bool = True,
+                     stream=None):
     """``attention`` with ``num_global`` global tokens beside the window (the
-    first positions read and are read by every row, under the causal mask).
-    ``workspace`` is a CUDA uint8 tensor of at least
-    ``attn_fwd_global_workspace_size`` bytes (allocated here when None)."""
+    first positions read and are read by every row, under the causal mask)."""
     import torch
     B, Hq, Nq, D = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
-        need = attn_fwd_global_workspace_size(B, Hq, Nq, D)
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
         if out is None:
             out = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
         if lse is None and return_lse:
             lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
         strides = [*q.stride(), *k.stride(), *v.stride(), *out.stride()]
-        ws_ptr = workspace.data_ptr() if workspace is not None else 0
-        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
         rc = attn_fwd_global(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                              lse.data_ptr() if lse is not None else 0, B, Hq, Hkv, Nq, Nk, D, _dtype_code(q), strides,
                              1 if causal else 0, int(window_left), int(window_right), int(num_global), float(scale),
-                             ws_ptr, ws_bytes, _stream_handle(stream))
+                             _stream_handle(stream))
     if rc != 0:
         raise EtattnError(rc, "attn_fwd_global")
     return out, lse
@@ -453,18 +436,14 @@ def attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, num_splits) -> int:
 
 def attn_fwd_varlen_global(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host,
                            num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal,
-                           window_left, window_right, num_global, scale, workspace, workspace_bytes, stream):
+                           window_left, window_right, num_global, scale, stream):
     """C ``attn_fwd_varlen_global``: pointers as ints; ``strides`` 12 ints."""
     lib = load_library()
     return lib.attn_fwd_varlen_global(q or None, k or None, v or None, o or None, lse or None, cu_seqlens_q or None,
                                       cu_seqlens_k or None, cu_seqlens_q_host or None, cu_seqlens_k_host or None,
                                       num_seqs, max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype,
                                       _strides_arg(strides), causal, window_left, window_right, num_global, scale,
-                                      workspace or None, workspace_bytes, stream or None)
-
-
-def attn_fwd_varlen_global_workspace_size(total_q, Hq, D) -> int:
-    return load_library().attn_fwd_varlen_global_workspace_size(total_q, Hq, D)
+                                      stream or None)
 
 
 def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = True, scale: float | None = None,
@@ -482,8 +461,8 @@ def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = Tru
     None).  Self-attention without a window goes through
     ``attn_fwd_varlen``, the rest through ``attn_fwd_varlen_ex``; with
     ``num_splits`` > 1 through ``attn_fwd_varlen_splitkv`` and with
-    ``num_global`` > 0 through ``attn_fwd_varlen_global`` (``workspace``: a
-    CUDA uint8 tensor of their workspace size, allocated here when None)."""
+    ``num_global`` > 0 through ``attn_fwd_varlen_global`` (``workspace``: the
+    split-KV scratch, a CUDA uint8 tensor allocated here when None)."""
     import torch
     T, Hq, D = q.shape
     Tk, Hkv = k.shape[0], k.shape[1]
@@ -516,8 +495,7 @@ def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = Tru
             if cu_seqlens_k is None:
                 host_k_ptr = host_ptr
             mk = int(max_seqlen if max_seqlen_k is None else max_seqlen_k)
-            need = (attn_fwd_varlen_global_workspace_size(T, Hq, D) if num_global > 0
-                    else attn_fwd_varlen_splitkv_workspace_size(T, Hq, D, int(num_splits)))
+            need = 0 if num_global > 0 else attn_fwd_varlen_splitkv_workspace_size(T, Hq, D, int(num_splits))
             if workspace is None and need > 0:
                 workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
             ws_ptr = workspace.data_ptr() if workspace is not None else 0
@@ -526,8 +504,7 @@ def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, causal: bool = Tru
                       cu_k.data_ptr(), host_ptr, host_k_ptr, S, int(max_seqlen), mk, T, Tk, Hq, Hkv, D,
                       _dtype_code(q), strides, 1 if causal else 0, int(window_left), int(window_right))
             if num_global > 0:
-                rc = attn_fwd_varlen_global(*common, int(num_global), float(scale), ws_ptr, ws_bytes,
-                                            _stream_handle(stream))
+                rc = attn_fwd_varlen_global(*common, int(num_global), float(scale), _stream_handle(stream))
                 name = "attn_fwd_varlen_global"
             else:
                 rc = attn_fwd_varlen_splitkv(*common, float(scale), int(num_splits), ws_ptr, ws_bytes,

@@ -214,7 +214,8 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
   const bool bf = dtype == ETATTN_BF16;
   const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
   const int64_t blocks1 = (tokens + 127) / 128, blocks2 = (tokens + 255) / 256;
-  const bool ksplit = splits == 1 && p.qpack == 1 && key_tiles >= 2 && 2 * blocks1 * (int64_t)gy * gz <= num_sms;
+  const bool ksplit = splits == 1 && p.qpack == 1 && p.num_global == 0 && key_tiles >= 2 &&
+                      2 * blocks1 * (int64_t)gy * gz <= num_sms;
   // Up to 128 query rows fill one sub-tile: a second one would only idle.
   const int nsub = (p.qpack > 1 || tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
   const int64_t gx = (ksplit || nsub == 1 ? blocks1 : blocks2) * splits;
@@ -363,7 +364,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
-  if (num_global < 0 || (num_global > 0 && (split == nullptr || split->num_splits != 2))) return ETATTN_ERR_BAD_SHAPE;
+  if (num_global < 0 || (num_global > 0 && split != nullptr)) return ETATTN_ERR_BAD_SHAPE;
   if (B == 0 || Hq == 0 || Nq == 0) return ETATTN_OK;  // empty output: nothing to do
   const bool has_keys = Nk > 0;
   if (!q || !o || (has_keys && (!k || !v))) return ETATTN_ERR_NULL_PTR;
@@ -408,7 +409,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // Equal lengths and no left bound: every row reads key 0, so the square
   // kernel applies whatever the right bound.  A split-KV slice can hold no
   // key of a row: the general build guards that.
-  const bool general = Nq != Nk || window_left_of(window_left) != kUnboundedWindow || splitting;
+  const bool general = Nq != Nk || window_left_of(window_left) != kUnboundedWindow || splitting || num_global > 0;
   const int qpack = qpack_of(general, Hq / Hkv, Nq);
 
   CUtensorMap mq, mk, mv;
@@ -449,9 +450,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   p.qpack = qpack;
-  // Global tokens: slice 1 of the split launch holds the global keys, slice 0
-  // the rest of each row's keys (the kernel's per-row key ranges).
-  p.num_global = splitting ? std::min(num_global, kMaxTokens) : 0;
+  // Global tokens: the global-token build streams each sub-tile's global keys,
+  // then the rest of its rows' keys (the kernel's per-row key ranges).
+  p.num_global = has_keys ? std::min(num_global, kMaxTokens) : 0;
   p.win_right_causal = causal ? 0 : kUnboundedWindow;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (splitting) {
@@ -686,7 +687,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   if (Hkv <= 0 || Hq % Hkv != 0) return ETATTN_ERR_BAD_HEADS;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ETATTN_ERR_BAD_SCALE;
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
-  if (num_global < 0 || (num_global > 0 && (split == nullptr || split->num_splits != 2))) return ETATTN_ERR_BAD_SHAPE;
+  if (num_global < 0 || (num_global > 0 && split != nullptr)) return ETATTN_ERR_BAD_SHAPE;
   if (split != nullptr && (split->num_splits < 1 || split->num_splits > kMaxSplits)) return ETATTN_ERR_BAD_SHAPE;
   if (cu_seqlens_q_host && !seqlens_ok(cu_seqlens_q_host, num_seqs, total_q, max_seqlen_q))
     return ETATTN_ERR_BAD_SEQLENS;
@@ -737,8 +738,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
   // Shared query and key offsets mean equal lengths in every sequence (see
   // fwd_impl for why the right bound does not matter).
-  const bool general =
-      cu_seqlens_k != cu_seqlens_q || window_left_of(window_left) != kUnboundedWindow || splitting;
+  const bool general = cu_seqlens_k != cu_seqlens_q || window_left_of(window_left) != kUnboundedWindow || splitting ||
+                       num_global > 0;
   const int qpack = qpack_of(general, Hq / Hkv, max_seqlen_q);
 
   CUtensorMap mq, mk, mv;
@@ -777,7 +778,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   p.status = status;
   p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0);
   p.qpack = qpack;
-  p.num_global = splitting ? std::min(num_global, kMaxTokens) : 0;
+  p.num_global = has_keys ? std::min(num_global, kMaxTokens) : 0;
   p.win_right_causal = causal ? 0 : kUnboundedWindow;
   const int64_t key_tiles = ((int64_t)max_seqlen_k + 127) / 128;
   if (splitting) {
@@ -840,22 +841,13 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
 
 int attn_fwd_global(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                     int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left,
-                    int window_right, int num_global, float scale, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                    int window_right, int num_global, float scale, void* stream) {
   if (num_global < 0) return ETATTN_ERR_BAD_SHAPE;
   // The window already holds every key the causal mask allows: nothing to add.
   const bool window_is_everything = window_left_of(window_left) == kUnboundedWindow &&
                                     window_right_of(window_right, causal) == (causal ? 0 : kUnboundedWindow);
-  if (num_global == 0 || window_is_everything)
-    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
-                    stream, true);
-  const SplitArgs sa{2, workspace, workspace_bytes};
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, dtype, strides, causal, window_left, window_right, scale,
-                  stream, true, &sa, num_global);
-}
-
-size_t attn_fwd_global_workspace_size(int B, int Hq, int Nq, int D) {
-  return attn_fwd_splitkv_workspace_size(B, Hq, Nq, D, 2);
+                  stream, true, nullptr, window_is_everything ? 0 : num_global);
 }
 
 // For callers that cannot allocate device memory at call time: a runtime
@@ -962,23 +954,13 @@ int attn_fwd_varlen_global(const void* q, const void* k, const void* v, void* o,
                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
                            const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
                            int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides,
-                           int causal, int window_left, int window_right, int num_global, float scale,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+                           int causal, int window_left, int window_right, int num_global, float scale, void* stream) {
   if (num_global < 0) return ETATTN_ERR_BAD_SHAPE;
   const bool window_is_everything = window_left_of(window_left) == kUnboundedWindow &&
                                     window_right_of(window_right, causal) == (causal ? 0 : kUnboundedWindow);
-  if (num_global == 0 || window_is_everything)
-    return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
-                       max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
-                       window_right, scale, stream, true);
-  const SplitArgs sa{2, workspace, workspace_bytes};
   return varlen_impl(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host, num_seqs,
                      max_seqlen_q, max_seqlen_k, total_q, total_k, Hq, Hkv, D, dtype, strides, causal, window_left,
-                     window_right, scale, stream, true, &sa, num_global);
-}
-
-size_t attn_fwd_varlen_global_workspace_size(int total_q, int Hq, int D) {
-  return attn_fwd_varlen_splitkv_workspace_size(total_q, Hq, D, 2);
+                     window_right, scale, stream, true, nullptr, window_is_everything ? 0 : num_global);
 }
 
 int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,

@@ -23,11 +23,11 @@ namespace etattn {
 
 namespace {
 
-template <int NSUB, bool GEN, bool KS>
+template <int NSUB, bool GEN, bool KS, bool GLB = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p, dim3 grid,
                        cudaStream_t stream) {
   using C = TileCfg<ETATTN_INST_D, NSUB>;
-  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0, GEN, KS>;
+  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0, GEN, KS, GLB>;
   // The dynamic shared-memory opt-in is per device; set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -68,6 +68,9 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 
 cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
                             dim3 grid, int nsub, bool general, bool ksplit, cudaStream_t stream) {
+  if (p.num_global > 0)  // global tokens: the general build with the two-phase tile stream
+    return nsub == 1 ? launch_one<1, true, false, true>(q, k, v, p, grid, stream)
+                     : launch_one<2, true, false, true>(q, k, v, p, grid, stream);
   if (ksplit) return launch_one<2, true, true>(q, k, v, p, grid, stream);
   if (general)
     return nsub == 1 ? launch_one<1, true, false>(q, k, v, p, grid, stream)

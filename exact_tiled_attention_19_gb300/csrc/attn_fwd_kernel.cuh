@@ -104,7 +104,7 @@ struct FwdParams {
   int64_t part_stride;           // rows per slice (the size of lse)
   int num_splits, split_tiles;   // key-tile slices; key tiles per slice
   int qpack;                     // query heads per 128-row sub-tile (1, or a power of two dividing group)
-  int num_global;                // global tokens (general build, two-slice split launch), else 0
+  int num_global;                // global tokens (the global-token build), else 0
   int win_right_causal;          // 0 under the causal mask, else kUnboundedWindow: the bound a global
                                  // token's connections keep
   float scale;                   // logit scale
@@ -187,26 +187,29 @@ struct Unit {
   int f0, f1;                    // first streamed tile read by sub-tile 0 / 1
   int n0, n1;                    // tiles read by sub-tile 0 / 1 (0 = nothing to read)
   int split;                     // key-tile slice of a split-KV launch (else 0)
+  int ng, wt0;                   // global-token build: streamed tiles of the global phase; key tile of
+                                 // the first window-phase tile (streamed tile ng)
+  int ga0, ga1;                  // global-token build: global-phase tiles read by sub-tile 0 / 1
   __device__ __forceinline__ int n(int s) const { return s ? n1 : n0; }
+  __device__ __forceinline__ int ga(int s) const { return s ? ga1 : ga0; }
   __device__ __forceinline__ int f(int s) const { return s ? f1 : f0; }
   // Sub-tile s reads streamed tile j.
   __device__ __forceinline__ bool reads(int s, int j) const { return (unsigned)(j - f(s)) < (unsigned)n(s); }
 };
 
-// Keys [lo, hi] (none when lo > hi) the row at key position c reads in this
-// launch.  Without global tokens: its window.  With G global tokens
-// ("Attention algorithms and data movement", lesson 07, global-token unions)
-// a row reads the global keys and its window, both under the causal mask
-// (limit h = c, or the last key), and a global row (c < G) reads every key
-// up to h.  That is two disjoint key intervals, computed as the two slices
-// of a split launch and merged: slice 1 holds [0, min(G - 1, h)], slice 0
-// the rest, [G, h] for a global row and the window clipped below at G
-// otherwise.  No key is counted in both.
-__device__ __forceinline__ int2 row_key_range(int c, const Unit& u, const FwdParams& p) {
+// Keys [lo, hi] (none when lo > hi) the row at key position c reads.
+// Without global tokens: its window.  With G global tokens ("Attention
+// algorithms and data movement", lesson 07, global-token unions) a row reads
+// the global keys and its window, both under the causal mask (limit h = c,
+// or the last key), and a global row (c < G) reads every key up to h.  That
+// is two disjoint key intervals, streamed as two phases: part 1, the global
+// keys [0, min(G - 1, h)]; part 0, the rest: [G, h] for a global row and the
+// window clipped below at G otherwise.  No key is counted in both.
+__device__ __forceinline__ int2 row_key_range(int c, const Unit& u, const FwdParams& p, int part) {
   int lo = max(0, c - p.win_left), hi = min(u.Lk - 1, c + p.win_right);
   if (p.num_global > 0) {
     const int G = p.num_global, h = min(u.Lk - 1, c + p.win_right_causal);
-    if (u.split == 1) {
+    if (part == 1) {
       lo = 0;
       hi = min(G - 1, h);
     } else if (c < G) {
@@ -224,10 +227,11 @@ __device__ __forceinline__ int2 row_key_range(int c, const Unit& u, const FwdPar
 // A row's first key never decreases with its position; its last key does
 // not either, except that a global row may end past the first non-global
 // row's window: the first and last rows' ranges bound every row's.
-__device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit& u, const FwdParams& p, int bn) {
+__device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit& u, const FwdParams& p, int bn,
+                                                   int part = 0) {
   if (r0 >= u.Lq) return make_int2(0, 0);
   const int c_first = r0 + u.delta, c_last = min(r0 + span - 1, u.Lq - 1) + u.delta;
-  const int2 a = row_key_range(c_first, u, p), b = row_key_range(c_last, u, p);
+  const int2 a = row_key_range(c_first, u, p, part), b = row_key_range(c_last, u, p, part);
   const int lo = min(a.x, b.x), hi = max(a.y, b.y);
   if (hi < lo) return make_int2(0, 0);
   return make_int2(lo / bn, hi / bn + 1);
@@ -240,7 +244,7 @@ __device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit&
 // too).  The first call, with j_to = 1, runs before the CTA's first barrier:
 // the Q and first K / V tiles are then in flight while tensor memory is
 // allocated; every later slot may still be in use and is waited for.
-template <int D, int NSUB, bool KS>
+template <int D, int NSUB, bool KS, bool GLB>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, SmemBarriers& sb, uint8_t* smem,
                                               const Unit u, int hn_swapped, int* status, int j_from, int j_to,
@@ -260,7 +264,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
   }
   int ks = j_from % C::K_STAGES, kph = (j_from / C::K_STAGES) & 1;  // K ring slot and its phase for tile j
   for (int j = j_from; j < min(j_to, u.n_tot); ++j) {
-    const int key0 = u.tok0k + (u.kt0 + j) * C::BN;
+    // Streamed tile j: key tile kt0 + j; in the global-token build the global
+    // phase's key tiles 0 .. ng - 1, then the window phase's from wt0 on.
+    const int key0 = u.tok0k + (GLB ? (j < u.ng ? j : u.wt0 + (j - u.ng)) : u.kt0 + j) * C::BN;
     // K_j goes to slot j % 3, whose previous tile j-3 must have been released.
     if (j >= C::K_STAGES && !mbar_wait(&sb.k_empty[ks], kph ^ 1, status)) return;
     {
@@ -351,7 +357,7 @@ __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int 
 // cycle the issuing thread spends elsewhere between groups is idle tensor time.
 // GEN = false is the square, window-free case, where both sub-tiles start at
 // streamed tile 0 and the per-tile range tests fold away at compile time.
-template <int D, int NSUB, bool GEN, bool KS>
+template <int D, int NSUB, bool GEN, bool KS, bool GLB>
 __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
   using C = TileCfg<D, NSUB>;
@@ -365,10 +371,20 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
   md.v1 = md.v0 + (uint64_t)(C::KV_BYTES >> 4);
   // Sub-tile `sub` reads streamed tile j; its own count of that tile.
   // Key split: sub-tile s reads the streamed tiles j = s mod 2.
+  // Global-token build: sub-tile s reads the global phase's streamed tiles
+  // 0 .. ga(s) - 1 and then n(s) - ga(s) window-phase tiles from f(s) on.
   auto reads = [&](int sub, int j) {
-    return KS ? ((j & 1) == sub && j < u.n_tot) : (GEN ? u.reads(sub, j) : j < u.n(sub));
+    if constexpr (GLB)
+      return j < u.ng ? j < u.ga(sub) : (unsigned)(j - u.f(sub)) < (unsigned)(u.n(sub) - u.ga(sub));
+    else
+      return KS ? ((j & 1) == sub && j < u.n_tot) : (GEN ? u.reads(sub, j) : j < u.n(sub));
   };
-  auto own = [&](int sub, int j) { return KS ? j >> 1 : (GEN ? j - u.f(sub) : j); };
+  auto own = [&](int sub, int j) {
+    if constexpr (GLB)
+      return j < u.ng ? j : u.ga(sub) + (j - u.f(sub));
+    else
+      return KS ? j >> 1 : (GEN ? j - u.f(sub) : j);
+  };
   if (u.n_tot == 0) return;  // no row of this CTA reads a key
   if (!mbar_wait(&sb.q_full, 0, status)) return;
 
@@ -473,7 +489,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // GEN = false is the square, window-free case: every row reads key 0 in the
 // first tile, so no row meets a tile with m = -inf and no lower edge exists.
-template <int D, int NSUB, bool BF16, bool GEN, bool KS>
+template <int D, int NSUB, bool BF16, bool GEN, bool KS, bool GLB>
 __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, const FwdParams& p, const Unit u,
                                              int s) {
   using C = TileCfg<D, NSUB>;
@@ -557,8 +573,18 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   const int c_row = row_pos + u.delta;
   const int kb0 = (u.kt0 + u.f(s)) * C::BN;
   int lim_hi, lim_lo;
-  if constexpr (GEN) {
-    const int2 kr = row_key_range(c_row, u, p);
+  int win_hi = 0, win_lo = 0;  // global-token build: the window phase's limits, taken up at tile ga(s)
+  if constexpr (GLB) {
+    // The global phase reads key tiles 0 .. ga(s) - 1 (limits of part 1), the
+    // window phase the tiles from wt0 + (f(s) - ng) on (limits of part 0).
+    const int2 kg = row_key_range(c_row, u, p, 1), kw = row_key_range(c_row, u, p, 0);
+    const int kbw = (u.wt0 + (u.f(s) - u.ng)) * C::BN;
+    win_hi = kw.y - kbw;
+    win_lo = kw.x - kbw;
+    lim_hi = u.ga(s) > 0 ? kg.y : win_hi;
+    lim_lo = u.ga(s) > 0 ? kg.x : win_lo;
+  } else if constexpr (GEN) {
+    const int2 kr = row_key_range(c_row, u, p, 0);
     lim_hi = kr.y - kb0;
     lim_lo = kr.x - kb0;
   } else {
@@ -566,6 +592,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     lim_lo = max(0, c_row - p.win_left) - kb0;
   }
   float m_run = -INFINITY;  // running maximum of the raw scores (scale > 0)
+  bool window_first = true;  // global-token build: no window-phase key of this row seen yet
   float l_run = 0.f;        // sum of exp2(c2 * (s - m_run)) over the keys seen
 
   for (int j = 0; j < n; ++j) {
@@ -619,6 +646,12 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     }
     lim_hi -= (KS ? 2 : 1) * C::BN;  // the key split's sub-tiles take every other tile
     lim_lo -= (KS ? 2 : 1) * C::BN;
+    if constexpr (GLB) {
+      if (j + 1 == u.ga(s)) {  // the next tile opens the window phase
+        lim_hi = win_hi;
+        lim_lo = win_lo;
+      }
+    }
 #pragma unroll
     for (int i = C::BN / 2; i < C::BN; i += 8) {
       mx0 = max3(mx0, sv[i], sv[i + 1]);
@@ -631,7 +664,19 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     // Lazy rescale: move the reference maximum only when it grows by more
     // than 8 in log2 units (always on the first tile, and always when the row
     // sees its first eligible key: -inf to finite compares as +inf > 8).
-    const bool rescale = (j == 0) || (m_new - m_run) * c2 > 8.f;
+    bool rescale = (j == 0) || (m_new - m_run) * c2 > 8.f;
+    // Global-token build: the global phase sets the reference maximum from the
+    // global keys alone, so the row's first window-phase tile that holds one
+    // of its keys takes up any larger maximum exactly; otherwise a small
+    // window's dominant key would enter P as a rounded value above 1 instead
+    // of exactly 1, and O would lose about a 16-bit rounding of its largest
+    // term.
+    if constexpr (GLB) {
+      if (j >= u.ga(s) && m_tile != -INFINITY) {
+        rescale = rescale || (window_first && m_new > m_run);
+        window_first = false;
+      }
+    }
     float alpha = 1.f;
     if (rescale) {
       alpha = (j == 0) ? 0.f : ex2_approx((m_run - m_new) * c2);
@@ -774,7 +819,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 // throughput configuration; NSUB = 1 gives small problems twice as many CTAs.
 // GEN = true handles unequal lengths and windows; the square, window-free
 // case compiles without their per-tile tests (they cost about 3% there).
-template <int D, int NSUB, bool BF16, bool GEN, bool KS>
+template <int D, int NSUB, bool BF16, bool GEN, bool KS, bool GLB>
 __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -857,7 +902,28 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   if (u.row0 >= u.Lq) active = false;
   u.delta = u.Lk - u.Lq;
   u.kt0 = u.n_tot = u.f0 = u.f1 = u.n0 = u.n1 = 0;
+  u.ng = u.wt0 = u.ga0 = u.ga1 = 0;
   if (!active) {
+  } else if (GLB) {
+    // Global tokens: each sub-tile streams the global keys' tiles (part 1,
+    // from key tile 0), then the tiles of the rest of its rows' keys (part 0).
+    // The CTA streams the longest global phase, then the union of the
+    // window phases; a tile holding both key G - 1 and later keys is read in
+    // both phases, masked to disjoint keys.
+    const int2 g0 = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN, 1);
+    const int2 g1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + u.span, u.span, u, p, C::BN, 1) : make_int2(0, 0);
+    const int2 w0 = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN, 0);
+    const int2 w1 = NSUB == 2 ? sub_tile_key_tiles(u.row0 + u.span, u.span, u, p, C::BN, 0) : make_int2(0, 0);
+    u.ga0 = g0.y;  // part 1 starts at key tile 0 (or is empty: {0, 0})
+    u.ga1 = g1.y;
+    u.ng = max(u.ga0, u.ga1);
+    const bool a0 = w0.y > w0.x, a1 = w1.y > w1.x;
+    u.wt0 = a0 ? (a1 ? min(w0.x, w1.x) : w0.x) : (a1 ? w1.x : 0);
+    u.n_tot = u.ng + ((a0 || a1) ? max(a0 ? w0.y : 0, a1 ? w1.y : 0) - u.wt0 : 0);
+    u.f0 = a0 ? u.ng + w0.x - u.wt0 : u.ng;
+    u.n0 = u.ga0 + (a0 ? w0.y - w0.x : 0);
+    u.f1 = a1 ? u.ng + w1.x - u.wt0 : u.ng;
+    u.n1 = u.ga1 + (a1 ? w1.y - w1.x : 0);
   } else if (KS) {  // one row block; sub-tile s takes the streamed tiles j = s mod 2
     const int2 r = sub_tile_key_tiles(u.row0, u.span, u, p, C::BN);
     u.kt0 = r.x;
@@ -886,7 +952,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   // are free and only this thread has touched the barriers yet.
   int k_issued = 0, v_issued = 0;  // key / value tiles the producer has issued
   if (producer && active)
-    producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1, k_issued, v_issued);
+    producer_role<D, NSUB, KS, GLB>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1, k_issued, v_issued);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -895,13 +961,13 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   if (!active) {
   } else if (warp < 4 * NSUB) {
     if constexpr (NSUB == 2) regs_grow<C::SOFTMAX_REGS>();
-    softmax_role<D, NSUB, BF16, GEN, KS>(sb, tmem, p, u, warp >> 2);
+    softmax_role<D, NSUB, BF16, GEN, KS, GLB>(sb, tmem, p, u, warp >> 2);
   } else {
     if constexpr (NSUB == 2) regs_shrink<C::CTRL_REGS>();
     const bool lane0 = (threadIdx.x & 31) == 0;
     if (warp == C::PRODUCER_WARP) {
       if (lane0) {
-        producer_role<D, NSUB, KS>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 1, 1 << 30, k_issued,
+        producer_role<D, NSUB, KS, GLB>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 1, 1 << 30, k_issued,
                                    v_issued);
         if (u.n_tot > 0) producer_settle<D, NSUB>(sb, k_issued, v_issued);
       }
@@ -911,7 +977,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
       if (lane0) {
-        mma_role<D, NSUB, GEN, KS>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+        mma_role<D, NSUB, GEN, KS, GLB>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
         // Every MMA this thread issued has completed before tensor memory is
         // released (immediate after a normal run; bounded after a wait ran out).
         mma_commit(&sb.fin);

@@ -175,27 +175,18 @@ size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Nq, int D, int num_spl
  * also read the global keys j < num_global, and a global row (key position
  * c < num_global) may read every key; both still obey the causal mask and
  * ignore the window.  Row i's eligible keys are the union of its window and
- * those connections, each key counted once.  The call runs one launch of two
- * key slices (the global keys; the rest) and the split-KV merge launch, so
- * the result equals the dense definition up to rounding order.
+ * those connections, each key counted once.  One launch streams, for every
+ * query tile, the global keys' tiles and then the rest of its rows' keys.
  *
  *   q, k, v, o, lse, strides, causal, windows, scale: as for attn_fwd_ex.
  *   num_global: >= 0.  With 0, or when the window already holds every key
  *           the causal mask allows (no left bound, and causal or no right
- *           bound), the call is attn_fwd_ex and the workspace is not used.
- *   workspace: as for attn_fwd_splitkv with num_splits = 2, at least
- *           attn_fwd_global_workspace_size(B, Hq, Nq, D) bytes.
- * Returns the codes of attn_fwd_splitkv; num_global < 0 is
- * ETATTN_ERR_BAD_SHAPE.
+ *           bound), the call is attn_fwd_ex.
+ * Returns the codes of attn_fwd_ex; num_global < 0 is ETATTN_ERR_BAD_SHAPE.
  */
 int attn_fwd_global(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                     int Nq, int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left,
-                    int window_right, int num_global, float scale, void* workspace, size_t workspace_bytes,
-                    void* stream);
-
-/* Bytes of workspace attn_fwd_global needs: attn_fwd_splitkv_workspace_size
- * with two slices (0 for invalid sizes). */
-size_t attn_fwd_global_workspace_size(int B, int Hq, int Nq, int D);
+                    int window_right, int num_global, float scale, void* stream);
 
 /*
  * attn_fwd_varlen_splitkv: attn_fwd_varlen_ex with the keys of every
@@ -230,20 +221,14 @@ int attn_fwd_varlen_splitkv_plan(int num_seqs, int Hq, int Hkv, int max_seqlen_q
 /*
  * attn_fwd_varlen_global: attn_fwd_varlen_ex plus num_global global tokens
  * per sequence (the first num_global positions of each sequence), with the
- * rule and the two-slice computation of attn_fwd_global.  The workspace
- * holds attn_fwd_varlen_global_workspace_size(total_q, Hq, D) bytes; with
- * num_global = 0, or a window that already holds every key the causal mask
- * allows, the call is attn_fwd_varlen_ex and the workspace is not used.
+ * rule of attn_fwd_global; with num_global = 0, or a window that already
+ * holds every key the causal mask allows, the call is attn_fwd_varlen_ex.
  */
 int attn_fwd_varlen_global(const void* q, const void* k, const void* v, void* o, float* lse,
                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host,
                            const int32_t* cu_seqlens_k_host, int num_seqs, int max_seqlen_q, int max_seqlen_k,
                            int total_q, int total_k, int Hq, int Hkv, int D, int dtype, const int64_t* strides,
-                           int causal, int window_left, int window_right, int num_global, float scale,
-                           void* workspace, size_t workspace_bytes, void* stream);
-
-/* Bytes of workspace attn_fwd_varlen_global needs (two slices). */
-size_t attn_fwd_varlen_global_workspace_size(int total_q, int Hq, int D);
+                           int causal, int window_left, int window_right, int num_global, float scale, void* stream);
 
 /* A split count for attn_fwd_splitkv on the current device: enough CTAs for
  * about four per SM when the query tiles alone do not fill the GPU, each

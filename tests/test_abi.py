@@ -254,24 +254,26 @@ def varlen_split_call(kind="split", num_splits=4, num_global=8, ws=0x70000000, w
               a["Tq"], a["Tk"], a["Hq"], a["Hkv"], a["D"], a["dtype"], st, a["causal"], a["wl"], a["wr"])
     if kind == "split":
         return B.attn_fwd_varlen_splitkv(*common, a["scale"], num_splits, ws, ws_bytes, a["stream"])
-    return B.attn_fwd_varlen_global(*common, num_global, a["scale"], ws, ws_bytes, a["stream"])
+    return B.attn_fwd_varlen_global(*common, num_global, a["scale"], a["stream"])
 
 
-def test_varlen_split_and_global_workspace_formulas():
+def test_varlen_splitkv_workspace_formula():
     rows = 100 * 4
     o_bytes = 3 * rows * 128 * 4
     padded = (o_bytes + 255) // 256 * 256
     assert B.attn_fwd_varlen_splitkv_workspace_size(100, 4, 128, 3) == padded + 3 * rows * 4
     assert B.attn_fwd_varlen_splitkv_workspace_size(100, 4, 128, 1) == 0
-    assert B.attn_fwd_varlen_global_workspace_size(100, 4, 128) == B.attn_fwd_varlen_splitkv_workspace_size(100, 4,
-                                                                                                            128, 2)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), 1), (dict(ws=0x70000010), 6), (dict(ws_bytes=1000), 3), (dict(ws=Q), 7),
+])
+def test_varlen_splitkv_workspace_errors(kw, code):
+    assert varlen_split_call("split", **kw) == code
 
 
 @pytest.mark.parametrize("kind", ["split", "global"])
-@pytest.mark.parametrize("kw,code", [
-    (dict(ws=0), 1), (dict(ws=0x70000010), 6), (dict(ws_bytes=1000), 3), (dict(ws=Q), 7),
-    (dict(Hkv=3), 4), (dict(cuk=0), 1), (dict(mk=-1), 3),
-])
+@pytest.mark.parametrize("kw,code", [(dict(Hkv=3), 4), (dict(cuk=0), 1), (dict(mk=-1), 3)])
 def test_varlen_split_and_global_invalid_arguments_rejected(kind, kw, code):
     assert varlen_split_call(kind, **kw) == code
 
@@ -285,7 +287,7 @@ def test_varlen_split_and_global_special_values():
     assert varlen_split_call("split") == want
     assert varlen_split_call("global") == want
     assert varlen_split_call("split", num_splits=1, ws=0, ws_bytes=0) == want   # one slice: no workspace
-    assert varlen_split_call("global", num_global=0, ws=0, ws_bytes=0) == want  # no global token: plain call
+    assert varlen_split_call("global", num_global=0) == want                    # no global token: plain call
     assert varlen_split_call("split", Tq=0) == 0
     rc, n = B.attn_fwd_varlen_splitkv_plan(8, 32, 8, 1, 32768)
     assert rc == want and (rc != 0 or n >= 1)
@@ -331,36 +333,29 @@ def test_splitkv_valid_calls_need_a_device():
     assert rc == want and (rc != 0 or n >= 1)
 
 
-def global_call(num_global=8, wl=32, wr=-1, ws=0x70000000, ws_bytes=1 << 30, **kw):
+def global_call(num_global=8, wl=32, wr=-1, **kw):
     a = good_args(**kw)
     Nk = kw.get("Nk", a["N"])
     st = (contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]) + contiguous_strides(a["B"], a["Hkv"], Nk, a["D"]) * 2
           + contiguous_strides(a["B"], a["Hq"], a["N"], a["D"]))
     return B.attn_fwd_global(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], Nk, a["D"],
-                             a["dtype"], st, a["causal"], wl, wr, num_global, a["scale"], ws, ws_bytes, a["stream"])
-
-
-def test_global_workspace_is_two_slices():
-    assert B.attn_fwd_global_workspace_size(2, 8, 3, 128) == B.attn_fwd_splitkv_workspace_size(2, 8, 3, 128, 2)
-    assert B.attn_fwd_global_workspace_size(2, 8, 3, 96) == 0
+                             a["dtype"], st, a["causal"], wl, wr, num_global, a["scale"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(num_global=-1), 3),
-    (dict(ws=0), 1), (dict(ws=0x70000010), 6), (dict(ws_bytes=1000), 3),
-    (dict(ws=Q), 7), (dict(Hkv=3), 4), (dict(N=-1), 3),
+    (dict(num_global=-1), 3), (dict(Hkv=3), 4), (dict(N=-1), 3), (dict(q=0), 1),
 ])
 def test_global_invalid_arguments_rejected(kw, code):
     assert global_call(**kw) == code
 
 
-def test_global_valid_calls_need_a_device_and_shortcuts_need_no_workspace():
+def test_global_valid_calls_need_a_device():
     import torch
     want = 12 if not torch.cuda.is_available() else 0
     assert global_call() == want
-    assert global_call(num_global=0, ws=0, ws_bytes=0) == want        # plain windowed call
-    assert global_call(wl=-1, ws=0, ws_bytes=0) == want               # causal, no left bound: the window is all
-    assert global_call(N=0) == 0                                       # no queries: no-op
+    assert global_call(num_global=0) == want        # plain windowed call
+    assert global_call(wl=-1) == want               # causal, no left bound: the window is all
+    assert global_call(N=0) == 0                    # no queries: no-op
 
 
 def noalloc_call(num_splits=4, **kw):

@@ -1,9 +1,9 @@
 """GPU parity of global tokens beside a local window (attn_fwd_global;
 "Attention algorithms and data movement", lesson 07, global-token unions).
 Every row also reads the first num_global keys and every global row reads
-all keys, both under the causal mask only; the kernel computes the global
-keys and the rest of each row's keys as two key slices and merges them, so
-each connection is counted once.  The result must match the FP64 oracle on
+all keys, both under the causal mask only; the kernel streams each query
+tile's global keys and then the rest of its rows' keys, so each connection is
+counted once.  The result must match the FP64 oracle on
 the same seeded inputs."""
 
 import numpy as np
@@ -25,10 +25,9 @@ def _device_status_clean():
     assert binding.etattn_read_device_status(clear=True) == 0
 
 
-def run_global(inp, G, causal, wl, wr, workspace=None):
+def run_global(inp, G, causal, wl, wr):
     q, k, v = (inp[n] if inp[n].is_cuda else rebuild_strided(inp[n]) for n in ("q", "k", "v"))
-    o, lse = binding.attention_global(q, k, v, num_global=G, causal=causal, window_left=wl, window_right=wr,
-                                      workspace=workspace)
+    o, lse = binding.attention_global(q, k, v, num_global=G, causal=causal, window_left=wl, window_right=wr)
     torch.cuda.synchronize()
     return o, lse
 
@@ -93,12 +92,10 @@ def test_global_more_than_every_key_is_causal_attention():
     compare_full(inp, o, lse, True, default_scale(64), torch.bfloat16)
 
 
-def test_global_workspace_reused_across_calls_is_bitwise_stable():
+def test_global_repeated_calls_are_bitwise_stable():
     inp = W.random_qkv(2, 4, 2, 600, 128, torch.bfloat16, seed=13)
-    need = binding.attn_fwd_global_workspace_size(2, 4, 600, 128)
-    ws = torch.full((need,), 0x7f, dtype=torch.uint8, device="cuda")  # garbage on entry
-    o1, l1 = run_global(inp, 48, True, 128, 0, workspace=ws)
-    o2, l2 = run_global(inp, 48, True, 128, 0, workspace=ws)
+    o1, l1 = run_global(inp, 48, True, 128, 0)
+    o2, l2 = run_global(inp, 48, True, 128, 0)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
