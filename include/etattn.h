@@ -28,7 +28,10 @@
  *     c_i - window_left <= j          (window_left  >= 0; negative = no bound)
  *     j <= c_i + window_right         (window_right >= 0; negative = no bound)
  * A row with no eligible key (Lk = 0, or Lq > Lk under the causal mask, or a
- * window past the keys) gets O_i = 0 and lse_i = -inf.
+ * window past the keys) gets O_i = 0 and lse_i = -inf.  The *_global entry
+ * points add global tokens (same page, lesson 07): with G of them, key j is
+ * also eligible when j < G, and every key when c_i < G, both still under the
+ * causal mask but not the window.
  *
  * Conventions shared by every entry point
  * ---------------------------------------

@@ -110,7 +110,7 @@ def test_rows_equal_unmasked_attention_over_the_key_slices(Lq, Lk, G, wl, wr, ca
 @pytest.mark.parametrize("G,wl,wr,causal", [(6, 4, 0, True), (10, 2, 3, False), (3, 0, 0, True)])
 def test_q_zero_closed_form(G, wl, wr, causal):
     """Q = 0: every eligible key has the same score, so O_i is the mean of the
-    values over the two slices and lse_i = ln(count)."""
+    values over the two key intervals and lse_i = ln(count)."""
     Lq = Lk = 40
     k, v = rnd((Lk, 4), 4), rnd((Lk, 4), 5)
     o, l = dense.attention_rows(np.zeros((Lq, 4)), k, v, np.arange(Lq), causal=causal, scale=1.0, window_left=wl,
