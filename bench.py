@@ -419,7 +419,7 @@ def cpu_baseline(w):
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
             "sample": desc + " (NumPy float64; BLAS matmuls multi-threaded, elementwise steps on one core)",
-            "seconds": dt}
+            "seconds": dt, "host_cores": len(os.sched_getaffinity(0)), "cpu_model": provenance_cpu_model()}
 
 
 def reference_arm(args, w, world, rank):
@@ -468,44 +468,33 @@ def workload_config(w, n_gpus):
 
 # ---------------------------------------------------------------- correctness gate and per-workload timing
 
-def correctness_gate(w, inp, dev):
-    """Every timed variant first matches the oracle: all elements for the small
-    workloads, sampled rows of a few heads for the large ones."""
+def correctness_gate(w, inp, dev, pool=None):
+    """Every timed variant first matches the oracle.  Small workloads: every
+    element.  Large ones: every (batch or sequence, head) on a stratified row
+    sample (the first and last 256 rows of each sequence and both rows at
+    every 128-row boundary), the oracle spread over the host cores.  Returns
+    (ok, max |dO|, max |dlse|) for the forward pass, (ok, worst error / bound,
+    None) for the backward pass."""
     import oracle
     import torch
+    from tests.oracle_pool import compare_workload, stratified_rows
     tol = 2e-3 if w.dtype == torch.float16 else 1e-2
     f64 = lambda t: t.float().double().cpu().numpy()
     if w.backward:
-        return backward_gate(w, inp, dev, f64)
+        ok, ratio = backward_gate(w, inp, dev, f64)
+        return ok, ratio, None
     o, lse = dev["o"], dev["lse"]
     if not bool(torch.isfinite(o).all()) or not bool(torch.isfinite(lse).all()):
-        return False, float("inf")
-    worst = 0.0
-    if w.layout == "varlen":
-        cu = inp["cu_seqlens"].tolist()
-        for s in (0, len(w.seqlens) - 1):
-            L, t0 = w.seqlens[s], cu[s]
-            rows = np.array(sorted({0, 1, 127, 128, L // 2, L - 1}))
-            rows = rows[rows < L]
-            ro, rl = oracle.attention_rows(f64(inp["q"][t0:t0 + L, 0]), f64(inp["k"][t0:t0 + L, 0]),
-                                           f64(inp["v"][t0:t0 + L, 0]), rows, causal=w.causal, scale=w.scale)
-            worst = max(worst, float(np.max(np.abs(f64(o[t0:t0 + L, 0][rows]) - ro))))
-            worst = max(worst, float(np.max(np.abs(f64(lse[0, t0:t0 + L][rows]) - rl))))
-    elif w.N * w.B * w.Hq <= 4096:
+        return False, float("inf"), float("inf")
+    if w.layout != "varlen" and w.N * w.B * w.Hq <= 4096:
         ro, rl = oracle.attention_dense(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), causal=w.causal, scale=w.scale,
                                         window_left=w.window_left, window_right=w.window_right,
                                         num_global=w.num_global)
-        worst = max(float(np.max(np.abs(f64(o) - ro))), float(np.max(np.abs(f64(lse) - rl))))
+        do, dl = float(np.max(np.abs(f64(o) - ro))), float(np.max(np.abs(f64(lse) - rl)))
     else:
-        rows = np.array(sorted({0, 1, 127, 128, w.N // 2, w.N - 1}))
-        for b, h in ((0, 0), (w.B - 1, w.Hq - 1)):
-            hk = h // (w.Hq // w.Hkv)
-            ro, rl = oracle.attention_rows(f64(inp["q"][b, h]), f64(inp["k"][b, hk]), f64(inp["v"][b, hk]), rows,
-                                           causal=w.causal, scale=w.scale, window_left=w.window_left,
-                                           window_right=w.window_right, num_global=w.num_global)
-            worst = max(worst, float(np.max(np.abs(f64(o[b, h][rows]) - ro))),
-                        float(np.max(np.abs(f64(lse[b, h][rows]) - rl))))
-    return worst <= tol, worst
+        r = compare_workload(w, inp, o.cpu(), lse.cpu(), rows_of=stratified_rows, pool=pool)
+        do, dl = r["max_abs_dO"], r["max_abs_dlse"]
+    return do <= tol and dl <= 1e-3, do, dl
 
 
 def backward_gate(w, inp, dev, f64):
@@ -530,45 +519,16 @@ def backward_gate(w, inp, dev, f64):
     return worst <= 1.0, worst
 
 
-def microbench(w, call, stream, samples=7, calls=20, warm=5):
-    """Page-style timing: 5 warm-up calls; 7 samples of 20 calls, median per
-    call; CUDA-graph replay and CUDA events as separate experiments."""
-    import torch
-    for _ in range(warm):
-        call()
-    torch.cuda.synchronize()
-    ev = []
-    for _ in range(samples):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(calls):
-            call()
-        b.record(stream)
-        b.synchronize()
-        ev.append(a.elapsed_time(b) * 1e3 / calls)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(calls):
-            call()
-    g.replay()
-    torch.cuda.synchronize()
-    gr = []
-    for _ in range(samples):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-        b.synchronize()
-        gr.append(a.elapsed_time(b) * 1e3 / calls)
-    del g
-    return {"us_event_median": statistics.median(ev), "us_event_min": min(ev), "us_event_max": max(ev),
-            "us_graph_median": statistics.median(gr), "us_graph_min": min(gr), "us_graph_max": max(gr)}
-
-
-def per_config_report(stream, device, peaks):
+def per_config_report(stream, device, peaks, pool, gated=None, samples=7, calls=20, warm=5, seed=0):
+    """Page-style timing of every workload: a correctness gate first; 5
+    warm-up calls; 7 samples of 20 calls each, per call the median (with min,
+    max and every raw sample kept), CUDA events and CUDA-graph replay as
+    separate experiments.  Every workload stays resident, and within each
+    sample the workloads run in a fresh random order (recorded)."""
     from exact_tiled_attention_19_gb300 import workloads as W
     import torch
-    out = {}
+    gated = gated or {}
+    out, live = {}, {}
     for name in PER_CONFIG:
         w = W.WORKLOADS[name]
         inp, dev = device_inputs(w, device)
@@ -576,24 +536,111 @@ def per_config_report(stream, device, peaks):
         with torch.cuda.stream(stream):
             call()
         torch.cuda.synchronize()
-        ok, err = correctness_gate(w, inp, dev)
-        entry = {"gate": "pass" if ok else "FAIL", "gate_max_abs_err": err}
-        if ok:
-            with torch.cuda.stream(stream):
-                m = microbench(w, call, stream)
-            us = m["us_graph_median"]
-            tf = w.flops() / (us * 1e-6) / 1e12
-            entry.update({k: round(v, 3) for k, v in m.items()})
-            entry["tflops_graph"] = round(tf, 2)
-            entry["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
-            entry["achieved_gbs_graph"] = round(w.io_bytes() / (us * 1e-6) / 1e9, 1)
-            entry["frac_of_hbm"] = round(entry["achieved_gbs_graph"] / peaks["hbm_gbs"], 4)
-            if w.splitkv:
-                entry["num_splits"] = dev["splits"]
+        ok, err, err_lse = gated[name] if name in gated else correctness_gate(w, inp, dev, pool)
+        entry = {"gate": "pass" if ok else "FAIL"}
+        if w.backward:
+            entry["gate_error_to_bound_ratio"] = err
+        else:
+            entry["gate_max_abs_dO"] = err
+            entry["gate_max_abs_dlse"] = err_lse
         out[name] = entry
-        del inp, dev
-        torch.cuda.empty_cache()
-    return out
+        del inp
+        if ok:
+            live[name] = (w, dev, call)
+    graphs, ev, gr = {}, {n: [] for n in live}, {n: [] for n in live}
+    with torch.cuda.stream(stream):
+        for name, (w, dev, call) in live.items():
+            for _ in range(warm):
+                call()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(calls):
+                    call()
+            g.replay()
+            graphs[name] = g
+        torch.cuda.synchronize()
+        rng = np.random.default_rng(seed)
+        orders = []
+        for _ in range(samples):
+            order = [str(n) for n in rng.permutation(list(live))]
+            orders.append(order)
+            for name in order:
+                call = live[name][2]
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(calls):
+                    call()
+                b.record(stream)
+                b.synchronize()
+                ev[name].append(a.elapsed_time(b) * 1e3 / calls)
+                a.record(stream)
+                graphs[name].replay()
+                b.record(stream)
+                b.synchronize()
+                gr[name].append(a.elapsed_time(b) * 1e3 / calls)
+    for name, (w, dev, call) in live.items():
+        e, g = ev[name], gr[name]
+        entry = out[name]
+        entry.update({"us_event_median": round(statistics.median(e), 3), "us_event_min": round(min(e), 3),
+                      "us_event_max": round(max(e), 3), "us_graph_median": round(statistics.median(g), 3),
+                      "us_graph_min": round(min(g), 3), "us_graph_max": round(max(g), 3),
+                      "us_event_samples": [round(x, 3) for x in e], "us_graph_samples": [round(x, 3) for x in g]})
+        us = entry["us_graph_median"]
+        tf = w.flops() / (us * 1e-6) / 1e12
+        entry["tflops_graph"] = round(tf, 2)
+        entry["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
+        entry["achieved_gbs_graph"] = round(w.io_bytes() / (us * 1e-6) / 1e9, 1)
+        entry["frac_of_hbm"] = round(entry["achieved_gbs_graph"] / peaks["hbm_gbs"], 4)
+        if w.splitkv:
+            entry["num_splits"] = dev["splits"]
+    del graphs, live
+    torch.cuda.empty_cache()
+    meta = {"samples": samples, "calls_per_sample": calls, "warmup_calls": warm, "order_seed": seed,
+            "variant_order_per_sample": orders}
+    return out, meta
+
+
+def provenance_cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    cpu_model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    cpu_model = line.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    try:
+        lscpu = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in lscpu.splitlines():
+            if line.startswith("Model name:"):
+                cpu_model = line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return cpu_model
+
+
+def provenance(device_index):
+    """Runtime metadata: source hashes, GPU and CPU names, host cores."""
+    import platform
+    import torch
+    csrc = os.path.join(ROOT, "exact_tiled_attention_19_gb300", "csrc")
+    every = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)) + ["../../include/etattn.h"]:
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                every.update(name.encode() + b"\0" + f.read())
+    return {"source_sha256": {**{k: kernel_source_digest(k) for k in KERNEL_SOURCES},
+                              "csrc_and_header": every.hexdigest()},
+            "bench_py_sha256": hashlib.sha256(open(os.path.abspath(__file__), "rb").read()).hexdigest(),
+            "gpu_name": torch.cuda.get_device_name(device_index), "cuda_runtime": torch.version.cuda,
+            "torch": torch.__version__, "cpu_model": provenance_cpu_model(),
+            "host_cores": len(os.sched_getaffinity(0)),
+            "python": platform.python_version()}
 
 
 def main():
@@ -608,6 +655,15 @@ def main():
             print(json.dumps(line), flush=True)
         return 0
 
+    # The oracle's process pool (correctness gates) is started with "spawn"
+    # before any GPU work, on the rank that gates.
+    from tests.oracle_pool import spawn_pool
+    from contextlib import nullcontext
+    with (spawn_pool() if rank == 0 else nullcontext()) as pool:
+        return run_ours(args, w, world, rank, local, pool)
+
+
+def run_ours(args, w, world, rank, local, pool):
     import torch
     from exact_tiled_attention_19_gb300 import binding
     binding.load_library()  # fails loudly if the CUDA library is missing
@@ -621,9 +677,10 @@ def main():
     with torch.cuda.stream(stream):
         call()
     torch.cuda.synchronize()
-    gate_ok, gate_err = correctness_gate(w, inp, dev)
-    if not gate_ok:
-        print(json.dumps({"metric": METRIC, "error": f"correctness gate failed (max abs err {gate_err})"}))
+    gate = correctness_gate(w, inp, dev, pool) if rank == 0 else (True, 0.0, 0.0)
+    if not gate[0]:
+        print(json.dumps({"metric": METRIC, "error": f"correctness gate failed (max |dO| or error/bound {gate[1]}, "
+                                                     f"max |dlse| {gate[2]})"}))
         return 1
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -650,9 +707,9 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
-    per_cfg = None
+    per_cfg = per_cfg_meta = None
     if rank == 0 and not args.no_per_config:
-        per_cfg = per_config_report(stream, device, peaks)
+        per_cfg, per_cfg_meta = per_config_report(stream, device, peaks, pool, gated={w.name: gate})
 
     if rank != 0:
         return 0
@@ -675,6 +732,7 @@ def main():
                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
                     "algorithmic_flops_per_launch": flops, "exact_causal_flops_per_launch": w.flops_exact(),
                     "algorithmic_bytes_per_launch": w.io_bytes(), "launch_ms_mean": round(launch_ms, 4)}
+    roofline["launch_ms_samples"] = [round(x, 4) for x in per_launch]
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
@@ -684,7 +742,13 @@ def main():
         "frac_of_bf16_peak": round(value / world / peaks["bf16_tflops"], 4),
         "roofline": roofline,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_call(w), "clocks": clocks,
-        "device_status": status, "per_config": per_cfg,
+        "device_status": status,
+        "correctness_gate": {"max_abs_dO" if not w.backward else "error_to_bound_ratio": gate[1],
+                             "max_abs_dlse": gate[2],
+                             "rows": "every element" if (w.layout != "varlen" and w.N * w.B * w.Hq <= 4096)
+                             else "every head; first and last 256 rows of each sequence and every 128-row boundary"},
+        "provenance": provenance(device.index),
+        "per_config": per_cfg, "per_config_timing": per_cfg_meta,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -9,7 +9,8 @@ The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_
 ``attn_fwd_varlen_global``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
-``etattn_read_device_status`` and ``etattn_version`` have the C names and
+``etattn_read_device_status``, ``etattn_selftest_wait_timeout`` and
+``etattn_version`` have the C names and
 arguments (pointers as ints).  The helpers ``attention`` and
 ``attention_varlen`` marshal torch CUDA tensors (output allocation, strides,
 the current stream) and call them; every step of the computation runs in the
@@ -35,6 +36,7 @@ STATUS_NAMES = {
     8: "ETATTN_ERR_BAD_SCALE", 9: "ETATTN_ERR_BAD_SEQLENS", 10: "ETATTN_ERR_LAUNCH", 11: "ETATTN_ERR_DEVICE",
     12: "ETATTN_ERR_NO_DEVICE",
 }
+globals().update({name: code for code, name in STATUS_NAMES.items()})
 
 
 class EtattnError(RuntimeError):
@@ -114,6 +116,8 @@ def load_library(path: str | None = None):
         lib.etattn_read_device_status.restype = _int
         lib.etattn_version.argtypes = []
         lib.etattn_version.restype = _int
+        lib.etattn_selftest_wait_timeout.argtypes = [_int, _vp]
+        lib.etattn_selftest_wait_timeout.restype = _int
         _lib = lib
         return lib
 
@@ -253,6 +257,13 @@ def etattn_read_device_status(clear: bool = True, stream: int = 0) -> int:
 
 def etattn_version() -> int:
     return load_library().etattn_version()
+
+
+def etattn_selftest_wait_timeout(limit_us: int, stream: int = 0) -> int:
+    """C ``etattn_selftest_wait_timeout``: enqueue the bounded-wait self-test
+    (a wait of limit_us microseconds that runs out and sets the device status
+    word).  Returns the status code."""
+    return load_library().etattn_selftest_wait_timeout(limit_us, stream or None)
 
 
 # ---------------------------------------------------------------- torch marshalling

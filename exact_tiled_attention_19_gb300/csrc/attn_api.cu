@@ -34,6 +34,19 @@ __device__ int g_status_word;
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
 
+// Self-test of the bounded waits: one thread waits, with the given limit, on
+// an mbarrier that nothing arrives at, through the same mbar_wait every
+// pipeline role uses.  The wait runs out and records kDevWaitTimeout in the
+// status word.  The kernel holds no tensor memory and starts no copy or MMA,
+// so its early return leaves nothing in flight.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  (void)mbar_wait(&bar, 0, status, limit_ns);
+}
+
 namespace {
 
 constexpr int kMaxTokens = 1 << 30;      // token coordinates stay well inside int32
@@ -220,17 +233,33 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
   const int nsub = (p.qpack > 1 || tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
   const int64_t gx = (ksplit || nsub == 1 ? blocks1 : blocks2) * splits;
   if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const dim3 g((unsigned)gx, gy, gz);
+  FwdParams pp = p;
+  pp.grid_x = (int)gx;
+  pp.grid_y = (int)gy;
+  pp.grid_z = (int)gz;
+  // Grouped longest-first dispatch (the kernel's cta_coords): groups of G
+  // (head, batch) pairs, G the smallest power of two whose CTAs fill the SMs
+  // once, so that the last group alone still spreads its shortest blocks over
+  // the GPU.  A grid too large for one dimension keeps the plain 3-D order.
+  dim3 g((unsigned)gx, gy, gz);
+  pp.sched_groups = 0;
+  const int64_t pairs = (int64_t)gy * gz;
+  if (gx * pairs <= 0x7fffffffLL) {
+    int64_t G = 1;
+    while (G * gx < num_sms && G < pairs) G *= 2;
+    pp.sched_groups = (int)((pairs + G - 1) / G);
+    g = dim3((unsigned)(gx * pairs), 1, 1);
+  }
   switch (D) {
     case 32:
-      return bf ? launch_fwd_d32_1(q, k, v, p, g, nsub, general, ksplit, s)
-                : launch_fwd_d32_0(q, k, v, p, g, nsub, general, ksplit, s);
+      return bf ? launch_fwd_d32_1(q, k, v, pp, g, nsub, general, ksplit, s)
+                : launch_fwd_d32_0(q, k, v, pp, g, nsub, general, ksplit, s);
     case 64:
-      return bf ? launch_fwd_d64_1(q, k, v, p, g, nsub, general, ksplit, s)
-                : launch_fwd_d64_0(q, k, v, p, g, nsub, general, ksplit, s);
+      return bf ? launch_fwd_d64_1(q, k, v, pp, g, nsub, general, ksplit, s)
+                : launch_fwd_d64_0(q, k, v, pp, g, nsub, general, ksplit, s);
     default:
-      return bf ? launch_fwd_d128_1(q, k, v, p, g, nsub, general, ksplit, s)
-                : launch_fwd_d128_0(q, k, v, p, g, nsub, general, ksplit, s);
+      return bf ? launch_fwd_d128_1(q, k, v, pp, g, nsub, general, ksplit, s)
+                : launch_fwd_d128_0(q, k, v, pp, g, nsub, general, ksplit, s);
   }
 }
 
@@ -861,7 +890,9 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
   if (B < 0 || Hq < 0 || Nq < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
   if (num_splits < 1 || num_splits > kMaxSplits) return ETATTN_ERR_BAD_SHAPE;
   const int64_t rows = (int64_t)B * Hq * Nq;
-  if (num_splits > 1 && rows > 0 &&
+  // Only a call that splits (more than one slice over at least one key)
+  // uses the scratch; without keys every row is empty and nothing is split.
+  if (num_splits > 1 && rows > 0 && Nk > 0 &&
       (splitkv_bytes(rows, D, num_splits) == 0 || splitkv_bytes(rows, D, num_splits) > kNoAllocScratchBytes))
     return ETATTN_ERR_BAD_SHAPE;  // beyond the fixed scratch
   // Every other argument is checked before the first device query.
@@ -1064,6 +1095,18 @@ int etattn_read_device_status(int* out, int clear, void* stream) {
   return ETATTN_OK;
 }
 
-int etattn_version(void) { return 200; }
+int etattn_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return ETATTN_ERR_BAD_SHAPE;
+  int dev = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status)) return rc;
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((unsigned long long)limit_us * 1000ull,
+                                                                         status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ETATTN_OK;
+}
+
+int etattn_version(void) { return 201; }
 
 }  // extern "C"

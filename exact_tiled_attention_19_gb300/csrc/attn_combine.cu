@@ -43,6 +43,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(CombineParams c) {
     for (int s = 0; s < c.num_splits; ++s) {
       const float ls = c.part_lse[(int64_t)s * c.rows + row];  // same address in every lane
       const float w = expf(ls - mx);                            // 0 for an empty slice
+      // A slice of weight 0 (no eligible key) adds nothing, and its partial
+      // row is not read: after a failed forward launch it may hold anything,
+      // and 0 * NaN would poison the merged row.  (w is the same in every lane.)
+      if (w == 0.f) continue;
       wsum += w;
       const float* src = c.part_o + ((int64_t)s * c.rows + row) * D + lane * PER;
       if constexpr (PER == 4) {

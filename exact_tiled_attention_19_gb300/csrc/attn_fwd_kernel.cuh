@@ -112,7 +112,41 @@ struct FwdParams {
   int* status;                   // device status word
   int hn_swapped;                // bit 0/1/2: the q/k/v tensor map orders (d, head, token, batch)
                                  // instead of (d, token, head, batch)
+  int grid_x, grid_y, grid_z;    // the logical grid: x = query block (x key slices) counted from the last,
+                                 // y = query head (pack), z = batch / sequence
+  int sched_groups;              // > 0: a 1-D launch of grid_x * grid_y * grid_z CTAs in grouped
+                                 // longest-first order (cta_coords); 0: the 3-D grid itself
 };
+
+// The logical (x, y, z) of this CTA.  The hardware starts CTAs in increasing
+// linear index.  With sched_groups = g > 0 the grid is launched 1-D and the
+// (y, z) pairs (y fastest) are cut into g contiguous groups of near-equal
+// size; a group's CTAs come one after another, ordered by x (so the longest
+// causal blocks of every pair of the group start first), then by pair.  The
+// CTAs running at any time then read the K/V of one group of heads, which
+// stays in L2, while the last CTAs to start are the shortest blocks of the
+// last group instead of a whole head's longest block (the causal tail).
+__device__ __forceinline__ int3 cta_coords(const FwdParams& p) {
+  if (p.sched_groups <= 0) return make_int3((int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z);
+  const long long gx = p.grid_x, lin = blockIdx.x;
+  const long long pairs = (long long)p.grid_y * p.grid_z;
+  const long long q = pairs / p.sched_groups, rem = pairs % p.sched_groups;  // group g holds q + (g < rem) pairs
+  // Each pair contributes gx CTAs, so CTA lin lies in the group holding the
+  // lin / gx-th pair.
+  const long long pi = lin / gx;
+  long long g, first;
+  if (pi < rem * (q + 1)) {
+    g = pi / (q + 1);
+    first = g * (q + 1);
+  } else {
+    g = rem + (pi - rem * (q + 1)) / q;
+    first = rem * (q + 1) + (g - rem) * q;
+  }
+  const long long size = q + (g < rem ? 1 : 0);
+  const long long r = lin - first * gx;
+  const long long pair = first + r % size;
+  return make_int3((int)(r / size), (int)(pair % p.grid_y), (int)(pair / p.grid_y));
+}
 
 // TMA load of one box at (d offset, token row, head, batch) for a map whose
 // middle axes may be ordered either way.
@@ -811,11 +845,11 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 }
 
 // ----------------------------------------------------------------- kernel
-// Grid: x = query block (NSUB * 128 rows) counted from the last one,
-// y = query head, z = batch (or sequence).  CTAs are dispatched in that order,
-// so the CTAs running at any time mostly belong to a few heads and share
-// their K/V tiles in L2, and within a head the longest causal rows start
-// first.  NSUB = 2 (two sub-tiles taking turns on the tensor core) is the
+// Logical grid: x = query block (NSUB * 128 rows) counted from the last one,
+// y = query head, z = batch (or sequence), dispatched in the grouped
+// longest-first order of cta_coords: the CTAs running at any time belong to
+// one group of heads and share its K/V tiles in L2, and within the group the
+// longest causal rows start first.  NSUB = 2 (two sub-tiles taking turns on the tensor core) is the
 // throughput configuration; NSUB = 1 gives small problems twice as many CTAs.
 // GEN = true handles unequal lengths and windows; the square, window-free
 // case compiles without their per-tile tests (they cost about 3% there).
@@ -866,11 +900,12 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
 
   // The CTA's work; `active` is uniform across the CTA.
   bool active = true;
+  const int3 cta = cta_coords(p);
   Unit u;
   u.P = GEN ? p.qpack : 1;
   u.span = C::BM / u.P;
-  u.h = blockIdx.y * u.P;
-  u.b = blockIdx.z;
+  u.h = cta.y * u.P;
+  u.b = cta.z;
   u.hk = u.h / p.group;
   u.Lq = p.Nq;
   u.Lk = p.Nk;
@@ -892,11 +927,11 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   }
   // x counts query blocks from the last one; in a split-KV launch the slices
   // of one block are adjacent.
-  int block = (int)gridDim.x - 1 - (int)blockIdx.x;
+  int block = p.grid_x - 1 - cta.x;
   u.split = 0;
   if (GEN && p.part_o != nullptr) {
-    u.split = (int)blockIdx.x % p.num_splits;
-    block = (int)(gridDim.x / p.num_splits) - 1 - (int)blockIdx.x / p.num_splits;
+    u.split = cta.x % p.num_splits;
+    block = p.grid_x / p.num_splits - 1 - cta.x / p.num_splits;
   }
   u.row0 = block * (KS ? 1 : NSUB) * u.span;
   if (u.row0 >= u.Lq) active = false;

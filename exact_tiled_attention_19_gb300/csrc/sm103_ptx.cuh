@@ -57,13 +57,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait until the phase with the given parity has completed. Returns false (and
-// records kDevWaitTimeout in *status) if it has not completed within the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+// records kDevWaitTimeout in *status) if it has not completed within limit_ns
+// of global time (kWaitLimitNs everywhere but the wait self-test).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0u && global_ns() - t0 > limit_ns) {
       if (status) atomicCAS(status, 0, (int)kDevWaitTimeout);
       return false;
     }

@@ -373,6 +373,23 @@ int etattn_last_cuda_error(void);
  */
 int etattn_read_device_status(int* out, int clear, void* stream);
 
+/*
+ * Self-test of the kernels' failure detection ("Intermediate and advanced
+ * extension", "Logic review before implementation": ordered launches, no
+ * spin barrier that could wait forever).  Every wait of the attention
+ * kernels' pipelines is bounded; this call checks that path on the device
+ * without disturbing a real launch.  It enqueues on `stream` one tiny kernel
+ * in which one thread waits, through the same bounded mbarrier wait as the
+ * pipelines but with a limit of limit_us microseconds, on a barrier that
+ * nothing arrives at.  The wait runs out and records a timeout in the device
+ * status word, so a following etattn_read_device_status reports
+ * ETATTN_ERR_DEVICE (and clears it when asked).  The kernel holds no tensor
+ * memory and starts no copy or MMA.  limit_us must lie in [1, 1000000].
+ * Returns ETATTN_OK, ETATTN_ERR_BAD_SHAPE (limit out of range),
+ * ETATTN_ERR_NO_DEVICE or ETATTN_ERR_LAUNCH.
+ */
+int etattn_selftest_wait_timeout(int limit_us, void* stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int etattn_version(void);
 

@@ -64,12 +64,12 @@ def derived_bound(ro, v_absmax, keys, dtype):
     return u * v_absmax + u * np.abs(ro) + sub + 1e-5
 
 
-def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True, window_left=-1, window_right=-1,
+def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=False, window_left=-1, window_right=-1,
                  num_global=0):
     """Compare every output element with the dense oracle.  The stated bounds
-    (max|dO| <= 2e-3 FP16 / 1e-2 BF16, max|d lse| <= 1e-3) must hold; for
-    shapes outside the five specified workloads (derived_ok) an O element may
-    instead meet the arithmetic bound of derived_bound.  Rows with no
+    (max|dO| <= 2e-3 FP16 / 1e-2 BF16, max|d lse| <= 1e-3) must hold.  Only a
+    caller that names its shape as an exception (derived_ok=True) lets an O
+    element meet the arithmetic bound of derived_bound instead.  Rows with no
     eligible key must be exact: O = 0 and lse = -inf."""
     q64, k64, v64 = to64(inputs["q"]), to64(inputs["k"]), to64(inputs["v"])
     win = dict(window_left=window_left, window_right=window_right, num_global=num_global)
@@ -107,8 +107,9 @@ def compare_full(inputs, o, lse, causal, scale, dtype, derived_ok=True, window_l
     if do > O_TOL[dtype]:
         bound = derived_bound(ro, vmax, keys, dtype)
         worst = float((err / bound).max())
-        more = f" and the arithmetic bound is exceeded ({worst:.3f}x)" if derived_ok else ""
-        assert derived_ok and worst <= 1.0, f"max|dO|={do} > {O_TOL[dtype]}" + more
+        i = np.unravel_index(int(err.argmax()), err.shape)
+        where = f" at {tuple(int(x) for x in i)} (|O_ref| = {abs(float(ro[i])):.4f}; {worst:.3f}x the arithmetic bound)"
+        assert derived_ok and worst <= 1.0, f"max|dO|={do} > {O_TOL[dtype]}" + where
     return do, dl
 
 

@@ -377,6 +377,9 @@ def test_noalloc_refuses_problems_beyond_its_scratch_before_any_device_work():
     assert noalloc_call(num_splits=0) == 3
     assert noalloc_call(num_splits=4, o=Q + 64) == 7
     assert noalloc_call(num_splits=4, N=0) == 0
+    # Without keys nothing is split and no scratch is used: a row count far
+    # beyond the scratch passes the size check (and then needs a device).
+    assert noalloc_call(num_splits=128, N=20000, Nk=0, k=0, v=0) == want
 
 
 DQ, DK, DV, DO, OO, WS = 0x80000000, 0x90000000, 0xA0000000, 0xB0000000, 0xC0000000, 0xD0000000
@@ -416,3 +419,12 @@ def test_bwd_workspace_and_empty_calls():
     want = 12 if not torch.cuda.is_available() else 0
     assert bwd_call() == want
     assert bwd_call(Nq=0, q=0, o=0, lse=0, dout=0, dq=0, ws=0, ws_bytes=0) == want  # no queries: dk = dv = 0
+
+
+def test_wait_selftest_checks_its_limit_before_any_device_work():
+    import torch
+    assert B.etattn_selftest_wait_timeout(0) == 3
+    assert B.etattn_selftest_wait_timeout(1000001) == 3
+    assert B.etattn_selftest_wait_timeout(1000) == (12 if not torch.cuda.is_available() else 0)
+    if torch.cuda.is_available():
+        B.etattn_read_device_status(clear=True)

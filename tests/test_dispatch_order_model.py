@@ -1,0 +1,111 @@
+"""CPU check of the forward kernel's CTA dispatch order (no GPU).
+
+A Python statement of the integer arithmetic of the launcher's group choice
+(attn_api.cu, launch) and the kernel's cta_coords (attn_fwd_kernel.cuh): the
+1-D launch index is mapped to the logical (x, y, z) of a CTA, with x the query
+block counted from the last, y the query head and z the batch or sequence.
+Checked here: the map is a bijection onto the logical grid; inside a group
+every CTA of a larger x (a shorter causal block) starts after every CTA of a
+smaller x; groups are contiguous ranges of (y, z) pairs of near-equal size.
+A list-scheduling model of the GPU (one CTA per SM, each SM taking the next
+CTA in launch order) shows the grouped order removing the causal tail of the
+plain 3-D order on the batched and packed workloads."""
+
+import heapq
+
+import pytest
+
+from exact_tiled_attention_19_gb300 import workloads as W
+
+SMS = 152
+
+
+def group_count(gx, gy, gz, num_sms=SMS):
+    """Groups of G (y, z) pairs, G the smallest power of two with
+    G * gx >= num_sms (or all pairs)."""
+    pairs = gy * gz
+    G = 1
+    while G * gx < num_sms and G < pairs:
+        G *= 2
+    return (pairs + G - 1) // G
+
+
+def cta_coords(lin, gx, gy, gz, groups):
+    pairs = gy * gz
+    q, rem = divmod(pairs, groups)
+    pi = lin // gx
+    if pi < rem * (q + 1):
+        g = pi // (q + 1)
+        first = g * (q + 1)
+    else:
+        g = rem + (pi - rem * (q + 1)) // q
+        first = rem * (q + 1) + (g - rem) * q
+    size = q + (1 if g < rem else 0)
+    r = lin - first * gx
+    pair = first + r % size
+    return r // size, pair % gy, pair // gy, g
+
+
+@pytest.mark.parametrize("gx,gy,gz", [(1, 1, 1), (16, 16, 4), (32, 32, 2), (59, 16, 16), (3, 7, 5), (2, 1000, 1),
+                                      (1, 152, 1), (5, 3, 1), (9, 11, 13), (4, 64, 1)])
+def test_cta_coords_is_a_bijection_longest_first_within_groups(gx, gy, gz):
+    groups = group_count(gx, gy, gz)
+    assert 1 <= groups <= gy * gz
+    seen = set()
+    last_x_of_group = {}
+    group_pairs = {}
+    for lin in range(gx * gy * gz):
+        x, y, z, g = cta_coords(lin, gx, gy, gz, groups)
+        assert 0 <= x < gx and 0 <= y < gy and 0 <= z < gz
+        assert (x, y, z) not in seen
+        seen.add((x, y, z))
+        # launch order inside a group: x never decreases
+        assert x >= last_x_of_group.get(g, 0)
+        last_x_of_group[g] = x
+        group_pairs.setdefault(g, set()).add(y + gy * z)
+    assert len(seen) == gx * gy * gz
+    sizes = [len(v) for v in group_pairs.values()]
+    assert max(sizes) - min(sizes) <= 1
+    # groups are contiguous pair ranges, in launch order
+    starts = [min(group_pairs[g]) for g in sorted(group_pairs)]
+    assert starts == sorted(starts)
+    for g in group_pairs:
+        ps = sorted(group_pairs[g])
+        assert ps == list(range(ps[0], ps[-1] + 1))
+
+
+def _causal_ctas(w, order):
+    """(launch order) list of per-CTA tile counts for a square causal workload
+    with two 128-row sub-tiles per CTA: block t streams tiles 0 .. 2t+1."""
+    lens = [lq for lq, _ in w.lengths()]
+    gx = max((L + 255) // 256 for L in lens)
+    gy, gz = w.Hq, len(lens)
+
+    def work(x, y, z):
+        L = lens[z]
+        t = gx - 1 - x
+        nb, kt = (L + 255) // 256, (L + 127) // 128
+        return min(2 * t + 2, kt) if t < nb else 0
+
+    if order == "grid":
+        return [work(x, y, z) for z in range(gz) for y in range(gy) for x in range(gx)]
+    groups = group_count(gx, gy, gz)
+    return [work(*cta_coords(lin, gx, gy, gz, groups)[:3]) for lin in range(gx * gy * gz)]
+
+
+def _makespan(tiles, fixed=2.0):
+    heap = [0.0] * SMS
+    for n in tiles:
+        t = heapq.heappop(heap)
+        heapq.heappush(heap, t + (fixed + n if n > 0 else 0.2))
+    return max(heap)
+
+
+@pytest.mark.parametrize("name,gain", [("b4_h16_n4096_d128_bf16", 0.10), ("gqa_b2_h32x8_n8192_d128_bf16", 0.05),
+                                       ("varlen16_h16_d128_bf16", 0.01)])
+def test_grouped_order_removes_the_causal_tail(name, gain):
+    w = W.WORKLOADS[name]
+    grid, grouped = _makespan(_causal_ctas(w, "grid")), _makespan(_causal_ctas(w, "grouped"))
+    ideal = sum(2.0 + n for n in _causal_ctas(w, "grid") if n > 0) / SMS
+    assert grouped <= grid * (1 - gain)
+    assert grouped <= ideal * 1.03
