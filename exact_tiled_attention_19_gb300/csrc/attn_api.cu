@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -205,6 +206,50 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
   return ETATTN_OK;
 }
 
+// (m, k) with floor(n / d) = (n * m) >> k for every n < 2^31 (the kernel's
+// div_magic): l = ceil(log2 d), k = 31 + l, m = ceil(2^k / d) < 2^32.
+void div_magic_of(uint32_t d, uint32_t* m, uint32_t* k) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  *k = 31 + l;
+  *m = (uint32_t)(((1ull << *k) + d - 1) / d);
+}
+
+// Keys read by the query row at key position c of a sequence with Lk keys
+// (the kernel's row_key_range, both parts): the window [c - wl, c + wr]
+// clipped to the keys; with G global tokens also the global keys [0, G) and,
+// for a global row (c < G), every key up to its causal limit (c + wrc).
+int64_t keys_of_row(int64_t c, int64_t Lk, int64_t wl, int64_t wr, int64_t wrc, int64_t G) {
+  const int64_t lo = std::max<int64_t>(0, c - wl), hi = std::min<int64_t>(Lk - 1, c + wr);
+  if (G <= 0) return std::max<int64_t>(0, hi - lo + 1);
+  const int64_t h = std::min<int64_t>(Lk - 1, c + wrc);
+  const int64_t glob = std::max<int64_t>(0, std::min<int64_t>(G - 1, h) + 1);
+  const int64_t rest = c < G ? std::max<int64_t>(0, h - G + 1) : std::max<int64_t>(0, hi - std::max(lo, G) + 1);
+  return glob + rest;
+}
+
+// Whether some query row of a sequence (Lq queries over Lk keys, bottom-right
+// aligned: row r at key position r + Lk - Lq) reads at least one and fewer
+// than kFewKeys keys, so that the kernel's split-P path may run.  The count is
+// piecewise linear in r, its pieces meeting where one clip of row_key_range
+// starts or stops binding; the smallest non-zero count is at the end of a
+// piece, so the first and last rows and the rows next to every breakpoint
+// decide it.
+bool has_few_key_rows(int64_t Lq, int64_t Lk, int64_t wl, int64_t wr, int64_t wrc, int64_t G) {
+  if (Lq <= 0 || Lk <= 0) return false;
+  const int64_t delta = Lk - Lq;
+  const int64_t cs[] = {0, wl, Lk - 1 - wr, Lk - 1 + wl, -wr, G - 1, G, G + wl, Lk - 1 - wrc, Lk - 1, G - wr};
+  std::vector<int64_t> rows = {0, Lq - 1};
+  for (int64_t c : cs)
+    for (int64_t d = -1; d <= 1; ++d) rows.push_back(c + d - delta);
+  for (int64_t r : rows) {
+    if (r < 0 || r >= Lq) continue;
+    const int64_t n = keys_of_row(r + delta, Lk, wl, wr, wrc, G);
+    if (n > 0 && n < kFewKeys) return true;
+  }
+  return false;
+}
+
 // Launch over `tokens` query rows per (head, batch/sequence).  Two 128-row
 // sub-tiles per CTA keep the tensor core busier, but halve the CTA count; a
 // problem that would not fill the GPU with two-sub-tile CTAs runs one
@@ -223,7 +268,7 @@ int encode_map(CUtensorMap* map, int dtype, const void* ptr, int D, int64_t n_to
 // sub-tiles taking alternate key tiles.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, bool general,
-                   cudaStream_t s, int64_t key_tiles = 0) {
+                   bool few_keys, cudaStream_t s, int64_t key_tiles = 0) {
   const bool bf = dtype == ETATTN_BF16;
   const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
   const int64_t blocks1 = (tokens + 127) / 128, blocks2 = (tokens + 255) / 256;
@@ -241,25 +286,30 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
   // (head, batch) pairs, G the smallest power of two whose CTAs fill the SMs
   // once, so that the last group alone still spreads its shortest blocks over
   // the GPU.  A grid too large for one dimension keeps the plain 3-D order.
+  // A grid that fits in one wave starts all at once: it keeps the 3-D order.
   dim3 g((unsigned)gx, gy, gz);
-  pp.sched_groups = 0;
+  pp.sched_q = pp.sched_rem = 0;
   const int64_t pairs = (int64_t)gy * gz;
-  if (gx * pairs <= 0x7fffffffLL) {
+  if (gx * pairs > num_sms && gx * pairs <= 0x7fffffffLL) {
     int64_t G = 1;
     while (G * gx < num_sms && G < pairs) G *= 2;
-    pp.sched_groups = (int)((pairs + G - 1) / G);
+    const int64_t groups = (pairs + G - 1) / G;  // near-equal groups: pairs / groups, the first pairs % groups one more
+    pp.sched_q = (int)(pairs / groups);
+    pp.sched_rem = (int)(pairs % groups);
+    const uint32_t divisors[4] = {(uint32_t)gx, (uint32_t)pp.sched_q + 1, (uint32_t)pp.sched_q, gy};
+    for (int i = 0; i < 4; ++i) div_magic_of(divisors[i], &pp.div_m[i], &pp.div_k[i]);
     g = dim3((unsigned)(gx * pairs), 1, 1);
   }
   switch (D) {
     case 32:
-      return bf ? launch_fwd_d32_1(q, k, v, pp, g, nsub, general, ksplit, s)
-                : launch_fwd_d32_0(q, k, v, pp, g, nsub, general, ksplit, s);
+      return bf ? launch_fwd_d32_1(q, k, v, pp, g, nsub, general, ksplit, few_keys, s)
+                : launch_fwd_d32_0(q, k, v, pp, g, nsub, general, ksplit, few_keys, s);
     case 64:
-      return bf ? launch_fwd_d64_1(q, k, v, pp, g, nsub, general, ksplit, s)
-                : launch_fwd_d64_0(q, k, v, pp, g, nsub, general, ksplit, s);
+      return bf ? launch_fwd_d64_1(q, k, v, pp, g, nsub, general, ksplit, few_keys, s)
+                : launch_fwd_d64_0(q, k, v, pp, g, nsub, general, ksplit, few_keys, s);
     default:
-      return bf ? launch_fwd_d128_1(q, k, v, pp, g, nsub, general, ksplit, s)
-                : launch_fwd_d128_0(q, k, v, pp, g, nsub, general, ksplit, s);
+      return bf ? launch_fwd_d128_1(q, k, v, pp, g, nsub, general, ksplit, few_keys, s)
+                : launch_fwd_d128_0(q, k, v, pp, g, nsub, general, ksplit, few_keys, s);
   }
 }
 
@@ -493,8 +543,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.num_splits = split->num_splits;
     p.split_tiles = (key_tiles + split->num_splits - 1) / split->num_splits;
   }
+  const bool few = dtype == ETATTN_BF16 && has_few_key_rows(Nq, Nk, p.win_left, p.win_right, p.win_right_causal,
+                                                            p.num_global);
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)Nq * qpack, (unsigned)(Hq / qpack), (unsigned)B, num_sms,
-                         general, st, (Nk + 127) / 128);
+                         general, few, st, (Nk + 127) / 128);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splitting) {
     CombineParams c{};
@@ -819,8 +871,17 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     p.split_tiles = (int)((key_tiles + split->num_splits - 1) / split->num_splits);
   }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Without host copies of the offsets any sequence may be short.
+  bool few = dtype == ETATTN_BF16;
+  if (few && cu_seqlens_q_host != nullptr && cu_seqlens_k_host != nullptr) {
+    few = false;
+    for (int i = 0; i < num_seqs && !few; ++i)
+      few = has_few_key_rows(cu_seqlens_q_host[i + 1] - cu_seqlens_q_host[i],
+                             cu_seqlens_k_host[i + 1] - cu_seqlens_k_host[i], p.win_left, p.win_right,
+                             p.win_right_causal, p.num_global);
+  }
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)max_seqlen_q * qpack, (unsigned)(Hq / qpack),
-                         (unsigned)num_seqs, num_sms, general, st, key_tiles);
+                         (unsigned)num_seqs, num_sms, general, few, st, key_tiles);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splitting) {
     CombineParams c{};

@@ -23,11 +23,11 @@ namespace etattn {
 
 namespace {
 
-template <int NSUB, bool GEN, bool KS, bool GLB = false>
+template <int NSUB, bool GEN, bool KS, bool GLB, bool SPL>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p, dim3 grid,
                        cudaStream_t stream) {
   using C = TileCfg<ETATTN_INST_D, NSUB>;
-  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0, GEN, KS, GLB>;
+  auto kern = attn_fwd_kernel<ETATTN_INST_D, NSUB, ETATTN_INST_BF16 != 0, GEN, KS, GLB, SPL>;
   // The dynamic shared-memory opt-in is per device; set it once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -66,17 +66,30 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 
 }  // namespace
 
-cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
-                            dim3 grid, int nsub, bool general, bool ksplit, cudaStream_t stream) {
+// The build with split = true carries the two-part P path for rows with few
+// keys (BF16 only; an FP16 call never asks for it).
+template <bool SPL>
+cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
+                           dim3 grid, int nsub, bool general, bool ksplit, cudaStream_t stream) {
   if (p.num_global > 0)  // global tokens: the general build with the two-phase tile stream
-    return nsub == 1 ? launch_one<1, true, false, true>(q, k, v, p, grid, stream)
-                     : launch_one<2, true, false, true>(q, k, v, p, grid, stream);
-  if (ksplit) return launch_one<2, true, true>(q, k, v, p, grid, stream);
+    return nsub == 1 ? launch_one<1, true, false, true, SPL>(q, k, v, p, grid, stream)
+                     : launch_one<2, true, false, true, SPL>(q, k, v, p, grid, stream);
+  if (ksplit) return launch_one<2, true, true, false, SPL>(q, k, v, p, grid, stream);
   if (general)
-    return nsub == 1 ? launch_one<1, true, false>(q, k, v, p, grid, stream)
-                     : launch_one<2, true, false>(q, k, v, p, grid, stream);
-  return nsub == 1 ? launch_one<1, false, false>(q, k, v, p, grid, stream)
-                   : launch_one<2, false, false>(q, k, v, p, grid, stream);
+    return nsub == 1 ? launch_one<1, true, false, false, SPL>(q, k, v, p, grid, stream)
+                     : launch_one<2, true, false, false, SPL>(q, k, v, p, grid, stream);
+  return nsub == 1 ? launch_one<1, false, false, false, SPL>(q, k, v, p, grid, stream)
+                   : launch_one<2, false, false, false, SPL>(q, k, v, p, grid, stream);
+}
+
+cudaError_t ETATTN_LAUNCHER(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
+                            dim3 grid, int nsub, bool general, bool ksplit, bool split, cudaStream_t stream) {
+#if ETATTN_INST_BF16
+  if (split) return launch_variant<true>(q, k, v, p, grid, nsub, general, ksplit, stream);
+#else
+  (void)split;
+#endif
+  return launch_variant<false>(q, k, v, p, grid, nsub, general, ksplit, stream);
 }
 
 }  // namespace etattn

@@ -114,38 +114,49 @@ struct FwdParams {
                                  // instead of (d, token, head, batch)
   int grid_x, grid_y, grid_z;    // the logical grid: x = query block (x key slices) counted from the last,
                                  // y = query head (pack), z = batch / sequence
-  int sched_groups;              // > 0: a 1-D launch of grid_x * grid_y * grid_z CTAs in grouped
-                                 // longest-first order (cta_coords); 0: the 3-D grid itself
+  int sched_q, sched_rem;        // sched_q > 0: a 1-D launch of grid_x * grid_y * grid_z CTAs in grouped
+                                 // longest-first order (cta_coords); the (y, z) pairs form groups of
+                                 // sched_q + 1 pairs (the first sched_rem groups) and sched_q pairs.
+                                 // sched_q = 0: the 3-D grid itself
+  uint32_t div_m[4];             // exact reciprocals (DivMagic) of grid_x, sched_q + 1, sched_q, grid_y
+  uint32_t div_k[4];
 };
 
+// Division of n < 2^31 by a divisor d >= 1 fixed at launch, as a multiply and
+// a shift: with l = ceil(log2 d), k = 31 + l and m = ceil(2^k / d) (which fits
+// in 32 bits), floor(n / d) = (n * m) >> k exactly.  Proof: n * m / 2^k =
+// n / d + n * e / (d * 2^k) with e = m * d - 2^k in [0, d), and
+// n * e < 2^31 * 2^l = 2^k, so the excess stays below 1 / d and cannot carry
+// the quotient past the next integer.  The host computes (m, k).
+__device__ __forceinline__ uint32_t div_magic(uint32_t n, uint32_t m, uint32_t k) {
+  return (uint32_t)(((uint64_t)n * m) >> k);
+}
+
 // The logical (x, y, z) of this CTA.  The hardware starts CTAs in increasing
-// linear index.  With sched_groups = g > 0 the grid is launched 1-D and the
-// (y, z) pairs (y fastest) are cut into g contiguous groups of near-equal
-// size; a group's CTAs come one after another, ordered by x (so the longest
-// causal blocks of every pair of the group start first), then by pair.  The
-// CTAs running at any time then read the K/V of one group of heads, which
-// stays in L2, while the last CTAs to start are the shortest blocks of the
-// last group instead of a whole head's longest block (the causal tail).
+// linear index.  With sched_q > 0 the grid is launched 1-D and the (y, z)
+// pairs (y fastest) are cut into contiguous groups of near-equal size; a
+// group's CTAs come one after another, ordered by x (so the longest causal
+// blocks of every pair of the group start first), then by pair.  The CTAs
+// running at any time then read the K/V of one group of heads, which stays in
+// L2, while the last CTAs to start are the shortest blocks of the last group
+// instead of a whole head's longest block (the causal tail).  The map runs at
+// every CTA's start, before any load is issued, so its divisions are
+// multiply-shifts (div_magic) rather than the general integer division.
 __device__ __forceinline__ int3 cta_coords(const FwdParams& p) {
-  if (p.sched_groups <= 0) return make_int3((int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z);
-  const long long gx = p.grid_x, lin = blockIdx.x;
-  const long long pairs = (long long)p.grid_y * p.grid_z;
-  const long long q = pairs / p.sched_groups, rem = pairs % p.sched_groups;  // group g holds q + (g < rem) pairs
+  if (p.sched_q <= 0) return make_int3((int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z);
+  const uint32_t lin = blockIdx.x, gx = (uint32_t)p.grid_x, gy = (uint32_t)p.grid_y;
+  const uint32_t q = (uint32_t)p.sched_q, big = (uint32_t)p.sched_rem * (q + 1);  // pairs in the larger groups
   // Each pair contributes gx CTAs, so CTA lin lies in the group holding the
-  // lin / gx-th pair.
-  const long long pi = lin / gx;
-  long long g, first;
-  if (pi < rem * (q + 1)) {
-    g = pi / (q + 1);
-    first = g * (q + 1);
-  } else {
-    g = rem + (pi - rem * (q + 1)) / q;
-    first = rem * (q + 1) + (g - rem) * q;
-  }
-  const long long size = q + (g < rem ? 1 : 0);
-  const long long r = lin - first * gx;
-  const long long pair = first + r % size;
-  return make_int3((int)(r / size), (int)(pair % p.grid_y), (int)(pair / p.grid_y));
+  // (lin / gx)-th pair.
+  const uint32_t pi = div_magic(lin, p.div_m[0], p.div_k[0]);
+  const bool large = pi < big;
+  const uint32_t size = large ? q + 1 : q, dm = large ? p.div_m[1] : p.div_m[2], dk = large ? p.div_k[1] : p.div_k[2];
+  const uint32_t first = large ? div_magic(pi, dm, dk) * size : big + div_magic(pi - big, dm, dk) * q;
+  const uint32_t r = lin - first * gx;
+  const uint32_t x = div_magic(r, dm, dk);
+  const uint32_t pair = first + (r - x * size);
+  const uint32_t z = div_magic(pair, p.div_m[3], p.div_k[3]);
+  return make_int3((int)x, (int)(pair - z * gy), (int)z);
 }
 
 // TMA load of one box at (d offset, token row, head, batch) for a map whose
@@ -188,7 +199,7 @@ struct TileCfg {
   // (TMA + MMA) shrinks to CTRL_REGS so that the two softmax warpgroups can
   // grow to SOFTMAX_REGS.  128*CTRL_REGS + 256*SOFTMAX_REGS <= 384*LAUNCH_REGS.
   static constexpr int LAUNCH_REGS = 168;
-  static constexpr int CTRL_REGS = 80;
+  static constexpr int CTRL_REGS = 88;
   static constexpr int SOFTMAX_REGS = 208;
   static_assert(NSUB == 1 || 128 * CTRL_REGS + 256 * SOFTMAX_REGS <= THREADS * LAUNCH_REGS,
                 "register split over budget");
@@ -205,6 +216,7 @@ struct SmemBarriers {
   uint64_t fin;                  // after a wait that ran out: every MMA issued so far has completed
   float merge_m[128], merge_l[128];  // key split: sub-tile 1's running max and sum per row
   uint32_t tmem_base;
+  uint32_t split_mask;           // bit s: sub-tile s takes P as two 16-bit parts (split_mask())
 };
 
 // Per-CTA work description shared by all roles.  Key tiles are streamed in
@@ -269,6 +281,49 @@ __device__ __forceinline__ int2 sub_tile_key_tiles(int r0, int span, const Unit&
   const int lo = min(a.x, b.x), hi = max(a.y, b.y);
   if (hi < lo) return make_int2(0, 0);
   return make_int2(lo / bn, hi / bn + 1);
+}
+
+// Sub-tiles with a row that reads fewer than kFewKeys keys take P at about
+// twice the input type's precision: P = P_hi + P_lo, both rounded to the input
+// type (P_lo the rounding residual of P_hi), and O gains both products.  Such
+// rows (the start of a causal sequence, a narrow window) hold few weights, so
+// one 16-bit rounding of a large weight would move O by up to a relative half
+// unit of the input type, on top of the output's own rounding; with many keys
+// the roundings average out: at 128 keys and more, a CPU model of this
+// kernel's arithmetic keeps every BF16 element of the batched, GQA and packed
+// causal workloads within 0.0078 of the exact result, the output rounding
+// itself.  Both ends of the sub-tile's valid rows bound the key counts in
+// between (a row's first and last keys never decrease with its position,
+// except for global rows, which read more keys).
+constexpr int kFewKeys = 128;
+__device__ __forceinline__ int few_keys(int r0, int span, const Unit& u, const FwdParams& p) {
+  if (r0 >= u.Lq) return 0;
+  int fewest = 1 << 30;
+  for (int end = 0; end < 2; ++end) {
+    const int c = (end ? min(r0 + span - 1, u.Lq - 1) : r0) + u.delta;
+    const int2 a = row_key_range(c, u, p, 0);
+    int cnt = max(0, a.y - a.x + 1);
+    if (p.num_global > 0) {
+      const int2 g = row_key_range(c, u, p, 1);
+      cnt += max(0, g.y - g.x + 1);
+    }
+    fewest = min(fewest, cnt);
+  }
+  return fewest < kFewKeys ? 1 : 0;
+}
+// Bit s set: sub-tile s takes the split P (the key split's two sub-tiles
+// hold the same rows).  One thread computes it at the CTA's set-up, after it
+// has issued the first loads (ahead of them it delays every CTA's start), and
+// the roles read it from shared memory.  A CTA with a split sub-tile runs the
+// SPLIT instantiation of its softmax and MMA roles; every other CTA runs code
+// without any trace of the second product.  The split code is only compiled
+// into the kernel (template SPL) that the host launches when some row of the
+// call may read fewer than kFewKeys keys, and only for BF16: FP16's 11-bit P
+// keeps the error within the FP16 bound.
+template <int NSUB, bool KS>
+__device__ __forceinline__ uint32_t split_mask(const Unit& u, const FwdParams& p) {
+  if (KS) return few_keys(u.row0, u.span, u, p) ? 3u : 0u;
+  return (uint32_t)few_keys(u.row0, u.span, u, p) | (NSUB == 2 ? (uint32_t)few_keys(u.row0 + u.span, u.span, u, p) << 1 : 0u);
 }
 
 // ----------------------------------------------------------------- producer
@@ -374,9 +429,13 @@ __device__ __forceinline__ void issue_s(const MmaDescs& md, uint32_t tmem, int s
 // O_s (+)= P_s V: A = P_s from tensor memory (8 cells = 16 keys per step),
 // B = V MN-major (d contiguous): 16 keys = 16 swizzled rows per step; LBO
 // steps between d-chunks, SBO between 8-row groups.
+// With split: then A = P_lo (columns [64, 128) of S_s) times the same V,
+// accumulated onto O_s.  That second product is rare (only sub-tiles with
+// few keys take it), so its loop is not unrolled: the issuing thread runs with
+// few registers, and unrolled it would hold eight more addresses.
 template <int D, int NSUB>
 __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int s, int st, bool accumulate,
-                                         uint32_t idesc) {
+                                         uint32_t idesc, bool split) {
   using C = TileCfg<D, NSUB>;
   const uint64_t vd = st ? md.v1 : md.v0;
   const uint32_t p_base = tmem + C::TM_S + s * 128;
@@ -385,13 +444,18 @@ __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int 
 #pragma unroll
   for (int kk = 0; kk < C::BN / 16; ++kk)
     mma_ts(d_tmem, p_base + kk * 8, vd + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), idesc, kk > 0 ? 1u : acc0);
+  if (split) {
+#pragma unroll 1
+    for (int kk = 0; kk < C::BN / 16; ++kk)
+      mma_ts(d_tmem, p_base + 64 + kk * 8, vd + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), idesc, 1u);
+  }
 }
 
 // Runs on one thread: the tensor pipe queues only a couple of MMAs, so any
 // cycle the issuing thread spends elsewhere between groups is idle tensor time.
 // GEN = false is the square, window-free case, where both sub-tiles start at
 // streamed tile 0 and the per-tile range tests fold away at compile time.
-template <int D, int NSUB, bool GEN, bool KS, bool GLB>
+template <int D, int NSUB, bool GEN, bool KS, bool GLB, bool SPLIT>
 __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32_t tmem, const Unit u,
                                          uint32_t idesc_s, uint32_t idesc_pv, int* status) {
   using C = TileCfg<D, NSUB>;
@@ -420,6 +484,7 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
       return KS ? j >> 1 : (GEN ? j - u.f(sub) : j);
   };
   if (u.n_tot == 0) return;  // no row of this CTA reads a key
+  const uint32_t split = SPLIT ? sb.split_mask : 0u;  // SPLIT = false: no second product anywhere
   if (!mbar_wait(&sb.q_full, 0, status)) return;
 
   if constexpr (KS) {
@@ -437,7 +502,7 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
               !mbar_wait(&sb.p_full[sub], (jl - 1) & 1, status))
             return;
           tc_fence_after();
-          issue_pv<D, NSUB>(md, tmem, sub, tp & 1, jl > 1, idesc_pv);
+          issue_pv<D, NSUB>(md, tmem, sub, tp & 1, jl > 1, idesc_pv, (split >> sub) & 1u);
           if (jl - 1 == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
           mma_commit(&sb.v_empty[tp & 1]);
         }
@@ -477,7 +542,7 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
         if (!mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.p_full[sub], li & 1, status))
           return;
         tc_fence_after();
-        issue_pv<D, NSUB>(md, tmem, sub, i & 1, li > 0, idesc_pv);
+        issue_pv<D, NSUB>(md, tmem, sub, i & 1, li > 0, idesc_pv, (split >> sub) & 1u);
         if (li == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
       }
       if (sub == 1) mma_commit(&sb.v_empty[i & 1]);  // every PV product of tile i is issued
@@ -520,10 +585,17 @@ template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
+template <bool BF16>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+  if constexpr (BF16)
+    unpack_bf16x2(w, lo, hi);
+  else
+    unpack_f16x2(w, lo, hi);
+}
 
 // GEN = false is the square, window-free case: every row reads key 0 in the
 // first tile, so no row meets a tile with m = -inf and no lower edge exists.
-template <int D, int NSUB, bool BF16, bool GEN, bool KS, bool GLB>
+template <int D, int NSUB, bool BF16, bool GEN, bool KS, bool GLB, bool SPLIT>
 __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, const FwdParams& p, const Unit u,
                                              int s) {
   using C = TileCfg<D, NSUB>;
@@ -601,6 +673,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   const uint32_t tS = tmem + C::TM_S + s * 128 + lane_off;
   const uint32_t tO = tmem + C::TM_O + s * 128 + lane_off;
   const float c2 = p.scale_log2;
+  constexpr bool split_p = SPLIT;  // the MMA thread adds the second product
   int* status = p.status;
   // Keys this row may read, as offsets from the first key of the current
   // tile: lim_lo <= i <= lim_hi.  Both move down by one tile per step.
@@ -723,20 +796,52 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     // the row sum in four independent pairs of accumulators.
     uint32_t pk[C::BN / 2];
     float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f, rc0 = 0.f, rc1 = 0.f, rd0 = 0.f, rd1 = 0.f;
+    // With split_p, P = P_hi + P_lo: P_hi goes over columns [0, 64) of S_s as
+    // usual; the residual P - P_hi, rounded, goes to columns [64, 128) (whose
+    // scores are in registers already), four columns at a time, and each half
+    // of P_hi is stored as soon as it is complete, so that the split path
+    // holds no more registers than the common one.
+    if constexpr (split_p) {
 #pragma unroll
-    for (int i = 0; i < C::BN / 2; i += 4) {
-      float x[8];
+      for (int i = 0; i < C::BN / 2; i += 4) {
+        float x[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
+        for (int k = 0; k < 4; ++k)
+          fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
-      add2(ra0, ra1, x[0], x[1]);
-      add2(rb0, rb1, x[2], x[3]);
-      add2(rc0, rc1, x[4], x[5]);
-      add2(rd0, rd1, x[6], x[7]);
+        for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
+        add2(ra0, ra1, x[0], x[1]);
+        add2(rb0, rb1, x[2], x[3]);
+        add2(rc0, rc1, x[4], x[5]);
+        add2(rd0, rd1, x[6], x[7]);
+        uint32_t r[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
+        for (int k = 0; k < 4; ++k) {
+          pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
+          float h0, h1, d0, d1;
+          unpack2<BF16>(pk[i + k], h0, h1);
+          fma2(d0, d1, h0, h1, -1.f, -1.f, x[2 * k], x[2 * k + 1]);
+          r[k] = pack2<BF16>(d0, d1);
+        }
+        tmem_st_x4(tS + 64 + i, r[0], r[1], r[2], r[3]);
+        if (i % 32 == 28) tmem_st_x32(tS + i - 28, pk + i - 28);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < C::BN / 2; i += 4) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
+        add2(ra0, ra1, x[0], x[1]);
+        add2(rb0, rb1, x[2], x[3]);
+        add2(rc0, rc1, x[4], x[5]);
+        add2(rd0, rd1, x[6], x[7]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
+      }
     }
     l_run = l_run * alpha + (((ra0 + rb0) + (rc0 + rd0)) + ((ra1 + rb1) + (rc1 + rd1)));
 
@@ -753,8 +858,10 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
         tmem_st_x32(tO + c, o);
       }
     }
-    tmem_st_x32(tS, pk);  // P_s(j) over the first 64 cells of S_s(j)
-    tmem_st_x32(tS + 32, pk + 32);
+    if constexpr (!split_p) {  // P_s(j) over the first 64 cells of S_s(j) (the split path stored it already)
+      tmem_st_x32(tS, pk);
+      tmem_st_x32(tS + 32, pk + 32);
+    }
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&sb.p_full[s]);
@@ -853,7 +960,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
 // throughput configuration; NSUB = 1 gives small problems twice as many CTAs.
 // GEN = true handles unequal lengths and windows; the square, window-free
 // case compiles without their per-tile tests (they cost about 3% there).
-template <int D, int NSUB, bool BF16, bool GEN, bool KS, bool GLB>
+template <int D, int NSUB, bool BF16, bool GEN, bool KS, bool GLB, bool SPL>
 __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -988,6 +1095,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   int k_issued = 0, v_issued = 0;  // key / value tiles the producer has issued
   if (producer && active)
     producer_role<D, NSUB, KS, GLB>(&tmQ, &tmK, &tmV, sb, smem, u, p.hn_swapped, p.status, 0, 1, k_issued, v_issued);
+  if (SPL && producer) sb.split_mask = active ? split_mask<NSUB, KS>(u, p) : 0u;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -996,7 +1104,10 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
   if (!active) {
   } else if (warp < 4 * NSUB) {
     if constexpr (NSUB == 2) regs_grow<C::SOFTMAX_REGS>();
-    softmax_role<D, NSUB, BF16, GEN, KS, GLB>(sb, tmem, p, u, warp >> 2);
+    if (SPL && ((sb.split_mask >> (warp >> 2)) & 1u))
+      softmax_role<D, NSUB, BF16, GEN, KS, GLB, SPL>(sb, tmem, p, u, warp >> 2);
+    else
+      softmax_role<D, NSUB, BF16, GEN, KS, GLB, false>(sb, tmem, p, u, warp >> 2);
   } else {
     if constexpr (NSUB == 2) regs_shrink<C::CTRL_REGS>();
     const bool lane0 = (threadIdx.x & 31) == 0;
@@ -1012,7 +1123,10 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
       constexpr uint32_t idesc_s = instr_desc_f16(128, C::BN, ab, false, false);
       constexpr uint32_t idesc_pv = instr_desc_f16(128, D, ab, false, true);
       if (lane0) {
-        mma_role<D, NSUB, GEN, KS, GLB>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+        if (SPL && sb.split_mask != 0u)
+          mma_role<D, NSUB, GEN, KS, GLB, SPL>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
+        else
+          mma_role<D, NSUB, GEN, KS, GLB, false>(sb, smem, tmem, u, idesc_s, idesc_pv, p.status);
         // Every MMA this thread issued has completed before tensor memory is
         // released (immediate after a normal run; bounded after a wait ran out).
         mma_commit(&sb.fin);

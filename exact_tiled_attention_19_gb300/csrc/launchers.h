@@ -11,7 +11,7 @@ struct FwdParams;
 
 #define ETATTN_DECLARE_LAUNCHER(name)                                                                     \
   cudaError_t name(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p, \
-                   dim3 grid, int nsub, bool general, bool ksplit, cudaStream_t stream);
+                   dim3 grid, int nsub, bool general, bool ksplit, bool split, cudaStream_t stream);
 
 ETATTN_DECLARE_LAUNCHER(launch_fwd_d32_0)
 ETATTN_DECLARE_LAUNCHER(launch_fwd_d32_1)

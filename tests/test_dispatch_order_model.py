@@ -20,42 +20,45 @@ from exact_tiled_attention_19_gb300 import workloads as W
 SMS = 152
 
 
-def group_count(gx, gy, gz, num_sms=SMS):
-    """Groups of G (y, z) pairs, G the smallest power of two with
-    G * gx >= num_sms (or all pairs)."""
+def group_sizes(gx, gy, gz, num_sms=SMS):
+    """(q, rem): groups of near-equal size, q + 1 pairs in the first rem
+    groups and q in the rest, with about G pairs each, G the smallest power
+    of two with G * gx >= num_sms (or all pairs)."""
     pairs = gy * gz
     G = 1
     while G * gx < num_sms and G < pairs:
         G *= 2
-    return (pairs + G - 1) // G
+    groups = (pairs + G - 1) // G
+    return pairs // groups, pairs % groups
 
 
-def cta_coords(lin, gx, gy, gz, groups):
-    pairs = gy * gz
-    q, rem = divmod(pairs, groups)
+def cta_coords(lin, gx, gy, gz, q, rem):
+    big = rem * (q + 1)
     pi = lin // gx
-    if pi < rem * (q + 1):
-        g = pi // (q + 1)
-        first = g * (q + 1)
+    if pi < big:
+        size = q + 1
+        first = pi // size * size
     else:
-        g = rem + (pi - rem * (q + 1)) // q
-        first = rem * (q + 1) + (g - rem) * q
-    size = q + (1 if g < rem else 0)
+        size = q
+        first = big + (pi - big) // q * q
     r = lin - first * gx
-    pair = first + r % size
-    return r // size, pair % gy, pair // gy, g
+    x = r // size
+    pair = first + (r - x * size)
+    z = pair // gy
+    return x, pair - z * gy, z, first
 
 
 @pytest.mark.parametrize("gx,gy,gz", [(1, 1, 1), (16, 16, 4), (32, 32, 2), (59, 16, 16), (3, 7, 5), (2, 1000, 1),
                                       (1, 152, 1), (5, 3, 1), (9, 11, 13), (4, 64, 1)])
 def test_cta_coords_is_a_bijection_longest_first_within_groups(gx, gy, gz):
-    groups = group_count(gx, gy, gz)
-    assert 1 <= groups <= gy * gz
+    q, rem = group_sizes(gx, gy, gz)
+    assert q >= 1 and 0 <= rem
     seen = set()
     last_x_of_group = {}
     group_pairs = {}
     for lin in range(gx * gy * gz):
-        x, y, z, g = cta_coords(lin, gx, gy, gz, groups)
+        x, y, z, g = cta_coords(lin, gx, gy, gz, q, rem)
+        assert lin < 2 ** 31 and g * gx <= lin
         assert 0 <= x < gx and 0 <= y < gy and 0 <= z < gz
         assert (x, y, z) not in seen
         seen.add((x, y, z))
@@ -89,8 +92,8 @@ def _causal_ctas(w, order):
 
     if order == "grid":
         return [work(x, y, z) for z in range(gz) for y in range(gy) for x in range(gx)]
-    groups = group_count(gx, gy, gz)
-    return [work(*cta_coords(lin, gx, gy, gz, groups)[:3]) for lin in range(gx * gy * gz)]
+    q, rem = group_sizes(gx, gy, gz)
+    return [work(*cta_coords(lin, gx, gy, gz, q, rem)[:3]) for lin in range(gx * gy * gz)]
 
 
 def _makespan(tiles, fixed=2.0):
@@ -109,3 +112,26 @@ def test_grouped_order_removes_the_causal_tail(name, gain):
     ideal = sum(2.0 + n for n in _causal_ctas(w, "grid") if n > 0) / SMS
     assert grouped <= grid * (1 - gain)
     assert grouped <= ideal * 1.03
+
+
+def div_magic_of(d):
+    """The launcher's (m, k): l = ceil(log2 d), k = 31 + l, m = ceil(2^k / d)."""
+    l = 0
+    while (1 << l) < d:
+        l += 1
+    k = 31 + l
+    return -(-(1 << k) // d), k
+
+
+@pytest.mark.parametrize("d", [1, 2, 3, 5, 7, 16, 59, 127, 152, 1000, 4097, 65535, 65536, 2 ** 20 + 1,
+                               2 ** 30 - 1, 2 ** 30 + 1, 2 ** 31 - 1])
+def test_multiply_shift_division_is_exact_below_2_31(d):
+    import random
+    m, k = div_magic_of(d)
+    assert 0 < m < 2 ** 32 and k <= 62
+    rng = random.Random(d)
+    ns = {0, 1, d - 1, d, d + 1, 2 ** 31 - 1, 2 ** 31 - 2} | {rng.randrange(2 ** 31) for _ in range(20000)}
+    ns |= {j * d + r for j in (1, 2, 1000, (2 ** 31 - 1) // d) for r in (0, d - 1) if j * d + r < 2 ** 31}
+    for n in ns:
+        if 0 <= n < 2 ** 31:
+            assert (n * m) >> k == n // d, (n, d)
