@@ -371,7 +371,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
       kph ^= 1;
     }
     const int vs = j & 1;
-    if (j >= 2 && !mbar_wait(&sb.v_empty[vs], ((j - 2) >> 1) & 1, status)) return;
+    // V_j's slot held V_(j-2).  The key split releases it on its own barrier;
+    // the other builds release it with step j - 1's commit on K_(j-1)'s slot.
+    if constexpr (KS) {
+      if (j >= 2 && !mbar_wait(&sb.v_empty[vs], ((j - 2) >> 1) & 1, status)) return;
+    } else {
+      if (j >= 2 && !mbar_wait(&sb.k_empty[(j - 1) % C::K_STAGES], ((j - 1) / C::K_STAGES) & 1, status)) return;
+    }
     {
       mbar_arrive_expect_tx(&sb.v_full[vs], C::KV_BYTES);
 #pragma unroll
@@ -531,21 +537,27 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
   ks = 1;
   // Step j issues the PV products of streamed tile j - 1 and the S products
   // of tile j, interleaved by sub-tile.
+  // The step's one release commit (on K_j's slot, after S_1(j)) also
+  // covers the PV products of tile j - 1 issued before it, so it frees V_(j-1)'s
+  // slot as well: the producer waits on it for V_(j+1) too.  Every wait and
+  // commit costs this thread a couple of hundred cycles of tensor idle time,
+  // so each step makes one release commit and waits for V only once.
   for (int j = 1; j <= u.n_tot; ++j) {
     const int i = j - 1;  // key tile whose PV products are issued in this step
     const bool has_k = j < u.n_tot;
     if (has_k && !mbar_wait(&sb.k_full[ks], kph, status)) return;
+    bool v_ready = false;
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub) {
       if (reads(sub, i)) {  // PV_sub(i)
         const int li = own(sub, i);
-        if (!mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status) || !mbar_wait(&sb.p_full[sub], li & 1, status))
-          return;
+        if (!v_ready && !mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status)) return;
+        v_ready = true;
+        if (!mbar_wait(&sb.p_full[sub], li & 1, status)) return;
         tc_fence_after();
         issue_pv<D, NSUB>(md, tmem, sub, i & 1, li > 0, idesc_pv, (split >> sub) & 1u);
         if (li == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
       }
-      if (sub == 1) mma_commit(&sb.v_empty[i & 1]);  // every PV product of tile i is issued
       if (has_k && reads(sub, j)) {  // S_sub(j)
         issue_s<D, NSUB>(md, tmem, sub, ks, idesc_s);
         mma_commit(&sb.s_full[sub]);
@@ -565,8 +577,9 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
   // arrival can land in shared memory after the CTA exits.
   for (int t = u.n_tot > C::K_STAGES ? u.n_tot - C::K_STAGES : 0; t < u.n_tot; ++t)
     if (!mbar_wait(&sb.k_empty[t % C::K_STAGES], (t / C::K_STAGES) & 1, status)) return;
-  for (int t = u.n_tot >= 2 ? u.n_tot - 2 : 0; t < u.n_tot; ++t)
-    if (!mbar_wait(&sb.v_empty[t & 1], (t >> 1) & 1, status)) return;
+  if constexpr (KS)
+    for (int t = u.n_tot >= 2 ? u.n_tot - 2 : 0; t < u.n_tot; ++t)
+      if (!mbar_wait(&sb.v_empty[t & 1], (t >> 1) & 1, status)) return;
 #pragma unroll
   for (int sub = 0; sub < 2; ++sub)
     if (u.n(sub) > 0 && !mbar_wait(&sb.o_done[sub], 0, status)) return;
