@@ -211,6 +211,7 @@ struct SmemBarriers {
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2];            // per sub-tile: S_s(j) is in tensor memory (and PV_s(j-1) is done)
   uint64_t p_full[2];            // per sub-tile: P_s(j) written and O_s corrected
+  uint64_t p_half[2];            // per sub-tile: the first half of P_s(j) (keys 0-63) written, O_s corrected
   uint64_t o_done[2];            // per sub-tile: last PV_s has completed
   uint64_t merge_ready;          // key split: sub-tile 1's (m, l) and O are final (128 arrivals)
   uint64_t fin;                  // after a wait that ran out: every MMA issued so far has completed
@@ -439,20 +440,23 @@ __device__ __forceinline__ void issue_s(const MmaDescs& md, uint32_t tmem, int s
 // accumulated onto O_s.  That second product is rare (only sub-tiles with
 // few keys take it), so its loop is not unrolled: the issuing thread runs with
 // few registers, and unrolled it would hold eight more addresses.
-template <int D, int NSUB>
+// H = 0 / 1 issues the steps of keys 0-63 / 64-127 only (released by p_half
+// and p_full), H = 2 all of them.
+template <int D, int NSUB, int H = 2>
 __device__ __forceinline__ void issue_pv(const MmaDescs& md, uint32_t tmem, int s, int st, bool accumulate,
                                          uint32_t idesc, bool split) {
   using C = TileCfg<D, NSUB>;
+  constexpr int K0 = H == 1 ? C::BN / 32 : 0, K1 = H == 0 ? C::BN / 32 : C::BN / 16;
   const uint64_t vd = st ? md.v1 : md.v0;
   const uint32_t p_base = tmem + C::TM_S + s * 128;
   const uint32_t d_tmem = tmem + C::TM_O + s * 128;
   const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
-  for (int kk = 0; kk < C::BN / 16; ++kk)
+  for (int kk = K0; kk < K1; ++kk)
     mma_ts(d_tmem, p_base + kk * 8, vd + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), idesc, kk > 0 ? 1u : acc0);
   if (split) {
 #pragma unroll 1
-    for (int kk = 0; kk < C::BN / 16; ++kk)
+    for (int kk = K0; kk < K1; ++kk)
       mma_ts(d_tmem, p_base + 64 + kk * 8, vd + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), idesc, 1u);
   }
 }
@@ -553,9 +557,12 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
         const int li = own(sub, i);
         if (!v_ready && !mbar_wait(&sb.v_full[i & 1], (i >> 1) & 1, status)) return;
         v_ready = true;
+        if (!mbar_wait(&sb.p_half[sub], li & 1, status)) return;
+        tc_fence_after();
+        issue_pv<D, NSUB, 0>(md, tmem, sub, i & 1, li > 0, idesc_pv, (split >> sub) & 1u);
         if (!mbar_wait(&sb.p_full[sub], li & 1, status)) return;
         tc_fence_after();
-        issue_pv<D, NSUB>(md, tmem, sub, i & 1, li > 0, idesc_pv, (split >> sub) & 1u);
+        issue_pv<D, NSUB, 1>(md, tmem, sub, i & 1, li > 0, idesc_pv, (split >> sub) & 1u);
         if (li == u.n(sub) - 1) mma_commit(&sb.o_done[sub]);
       }
       if (has_k && reads(sub, j)) {  // S_sub(j)
@@ -673,6 +680,7 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
   if (!__any_sync(FULL, valid)) {
     for (int j = 0; j < n; ++j) {
       if (!warp_wait(&sb.s_full[s], j & 1, p.status)) return;
+      if constexpr (!KS) mbar_arrive(&sb.p_half[s]);
       mbar_arrive(&sb.p_full[s]);
     }
     if (KS && s == 1) {
@@ -805,76 +813,68 @@ __device__ __forceinline__ void softmax_role(SmemBarriers& sb, uint32_t tmem, co
     // A row that has not met an eligible key yet keeps m = -inf; its masked
     // scores must still give p = exp2(-inf) = 0, not exp2(-inf + inf).
     const float neg_mc = (GEN && m_run == -INFINITY) ? 0.f : -m_run * c2;
+    // Correction: O_s *= alpha for rows whose maximum moved.  PV_s(j-1) has
+    // completed: the commit that signalled S_s(j) covers it.  It comes before
+    // any part of P_s(j) is released, since the PV products add onto O_s.
+    // (Sixteen columns at a time: the scores are still held in registers.)
+    if (j > 0 && __any_sync(FULL, rescale)) {
+#pragma unroll 1
+      for (int c = 0; c < D; c += 16) {
+        uint32_t o[16];
+        tmem_ld_x16(tO + c, o);
+        tmem_ld_wait16(o);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st_x16(tO + c, o);
+      }
+    }
     // p = exp2(s * c2 - m * c2): the scaling runs two lanes per instruction,
-    // the row sum in four independent pairs of accumulators.
+    // the row sum in four independent pairs of accumulators.  P_s(j) goes
+    // over the first 64 cells of S_s(j) in two halves: keys 0-63 are stored as
+    // soon as they are ready and released on p_half, so that the first half of
+    // the PV product runs on the tensor core while keys 64-127 are computed
+    // (the release waits two more steps of the loop, hiding the stores).
+    // With split_p, P = P_hi + P_lo: the residual P - P_hi, rounded, goes to
+    // columns [64, 128) (whose scores are in registers already), four columns
+    // at a time, so that no array of it is held.
     uint32_t pk[C::BN / 2];
     float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f, rc0 = 0.f, rc1 = 0.f, rd0 = 0.f, rd1 = 0.f;
-    // With split_p, P = P_hi + P_lo: P_hi goes over columns [0, 64) of S_s as
-    // usual; the residual P - P_hi, rounded, goes to columns [64, 128) (whose
-    // scores are in registers already), four columns at a time, and each half
-    // of P_hi is stored as soon as it is complete, so that the split path
-    // holds no more registers than the common one.
-    if constexpr (split_p) {
 #pragma unroll
-      for (int i = 0; i < C::BN / 2; i += 4) {
-        float x[8];
+    for (int i = 0; i < C::BN / 2; i += 4) {
+      float x[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
+      for (int k = 0; k < 4; ++k)
+        fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
-        add2(ra0, ra1, x[0], x[1]);
-        add2(rb0, rb1, x[2], x[3]);
-        add2(rc0, rc1, x[4], x[5]);
-        add2(rd0, rd1, x[6], x[7]);
+      for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
+      add2(ra0, ra1, x[0], x[1]);
+      add2(rb0, rb1, x[2], x[3]);
+      add2(rc0, rc1, x[4], x[5]);
+      add2(rd0, rd1, x[6], x[7]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
+      if constexpr (split_p) {
         uint32_t r[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
           float h0, h1, d0, d1;
           unpack2<BF16>(pk[i + k], h0, h1);
           fma2(d0, d1, h0, h1, -1.f, -1.f, x[2 * k], x[2 * k + 1]);
           r[k] = pack2<BF16>(d0, d1);
         }
         tmem_st_x4(tS + 64 + i, r[0], r[1], r[2], r[3]);
-        if (i % 32 == 28) tmem_st_x32(tS + i - 28, pk + i - 28);
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < C::BN / 2; i += 4) {
-        float x[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          fma2(x[2 * k], x[2 * k + 1], sv[2 * (i + k)], sv[2 * (i + k) + 1], c2, c2, neg_mc, neg_mc);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = ex2_approx(x[k]);
-        add2(ra0, ra1, x[0], x[1]);
-        add2(rb0, rb1, x[2], x[3]);
-        add2(rc0, rc1, x[4], x[5]);
-        add2(rd0, rd1, x[6], x[7]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pk[i + k] = pack2<BF16>(x[2 * k], x[2 * k + 1]);
+      if (i == 28) tmem_st_x32(tS, pk);  // keys 0-63
+      if constexpr (!KS) {
+        if (i == 36) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&sb.p_half[s]);
+        }
       }
     }
     l_run = l_run * alpha + (((ra0 + rb0) + (rc0 + rd0)) + ((ra1 + rb1) + (rc1 + rd1)));
-
-    // Correction: O_s *= alpha for rows whose maximum moved.  PV_s(j-1) has
-    // completed: the commit that signalled S_s(j) covers it.
-    if (j > 0 && __any_sync(FULL, rescale)) {
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + c, o);
-        tmem_ld_wait32(o);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st_x32(tO + c, o);
-      }
-    }
-    if constexpr (!split_p) {  // P_s(j) over the first 64 cells of S_s(j) (the split path stored it already)
-      tmem_st_x32(tS, pk);
-      tmem_st_x32(tS + 32, pk + 32);
-    }
+    tmem_st_x32(tS + 32, pk + 32);  // keys 64-127
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&sb.p_full[s]);
@@ -1002,6 +1002,7 @@ __global__ void __launch_bounds__(TileCfg<D, NSUB>::THREADS, 1)
       mbar_init(&sb.v_empty[i], 1);
       mbar_init(&sb.s_full[i], 1);
       mbar_init(&sb.p_full[i], 128);
+      mbar_init(&sb.p_half[i], 128);
       mbar_init(&sb.o_done[i], 1);
     }
     mbar_init(&sb.merge_ready, 128);

@@ -8,11 +8,13 @@ A discrete-event restatement of attn_fwd_kernel.cuh's roles and mbarriers:
   other builds with step j - 1's release commit on K_(j-1)'s slot;
 * the MMA issuer (one thread, mma_role): step 0 issues S_s(0) for each
   sub-tile that reads tile 0; step j >= 1 waits for K_j, then per sub-tile the
-  PV of tile j - 1 (after V_(j-1), waited once per step, and that sub-tile's
-  P) and S of tile j, and makes one release commit on K_j's slot; the
+  PV of tile j - 1 (after V_(j-1), waited once per step; its first half after
+  that sub-tile's first half of P, the rest after all of P) and S of tile j,
+  and makes one release commit on K_j's slot; the
   key-split build runs its own loop (alternate tiles per sub-tile, PV's V
   release per tile);
-* one softmax group per sub-tile: waits for each of its S, arrives its P.
+* one softmax group per sub-tile: waits for each of its S, releases the
+  first half of its P, then all of it (the key split: all of it at once).
 
 Commits arrive when every earlier tensor operation has left the tensor pipe,
 which runs them in issue order.  Loads complete after random delays, and the
@@ -74,6 +76,7 @@ def run(n_tot, reads, ks_build, seed, v_step_back=1):
         bars[f"v_full{i}"], bars[f"v_empty{i}"] = Barrier(1), Barrier(1)
     for s in range(2):
         bars[f"s_full{s}"], bars[f"p_full{s}"], bars[f"o_done{s}"] = Barrier(1), Barrier(1), Barrier(1)
+        bars[f"p_half{s}"] = Barrier(1)
     pipe, inflight = [], []
     k_slot, v_slot = [None] * K_ST, [None] * V_ST
     left = {}      # ("k" | "v", tile) -> number of products reading it that left the pipe
@@ -150,6 +153,8 @@ def run(n_tot, reads, ks_build, seed, v_step_back=1):
                         if not v_ready:
                             yield from wait(f"v_full{i % V_ST}", i // V_ST)
                         v_ready = True
+                        yield from wait(f"p_half{s}", own[s][i])
+                        mma("pv_first_half", s, i)
                         yield from wait(f"p_full{s}", own[s][i])
                         mma("pv", s, i)
                         if own[s][i] == len(reads[s]) - 1:
@@ -174,6 +179,10 @@ def run(n_tot, reads, ks_build, seed, v_step_back=1):
             yield from wait(f"s_full{s}", li)
             for _ in range(rng.randint(0, 3)):
                 yield
+            if not ks_build:
+                bars[f"p_half{s}"].arrive()
+                for _ in range(rng.randint(0, 3)):
+                    yield
             bars[f"p_full{s}"].arrive()
         if reads[s]:
             yield from wait(f"o_done{s}", 0)
@@ -182,11 +191,11 @@ def run(n_tot, reads, ks_build, seed, v_step_back=1):
         while True:
             if pipe and rng.random() < 0.6:
                 kind, op, what = pipe.pop(0)
-                if kind == "mma":
+                if kind == "commit":
+                    bars[what].arrive()
+                elif op != "pv_first_half":
                     key = ("k" if op == "s" else "v", what)
                     left[key] = left.get(key, 0) + 1
-                else:
-                    bars[what].arrive()
             yield
 
     def loads():
@@ -216,6 +225,8 @@ def run(n_tot, reads, ks_build, seed, v_step_back=1):
         mine = [e for e in events if e[0] == s]
         for a, b in zip(reads[s], reads[s][1:]):
             assert mine.index((s, "pv", a)) < mine.index((s, "s", b))
+            if not ks_build:
+                assert mine.index((s, "pv_first_half", a)) < mine.index((s, "pv", a))
         if reads[s]:
             assert (s, "pv", reads[s][-1]) in mine
 
