@@ -36,11 +36,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak; µs/call (1 GPU)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-PER_CONFIG = ["n129_d32_f16_causal", "n512_d64_f16_causal", "n512_d64_f16_noncausal", "n512_d64_f16_causal_qx30",
-              "b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd", "gqa_b2_h32x8_n8192_d128_bf16",
-              "varlen16_h16_d128_bf16", "chunk2048_cache16384_gqa", "window4096_n16384",
-              "global64_window4096_n16384", "decode_b8_h32x8_k32768",
-              "bwd_b4_h16_n4096_d128_bf16", "bwd_gqa_b2_h32x8_n8192_d128_bf16"]
+# Per-workload timing, by family: the workloads of one family are variants of one problem (a
+# layout, a mask, a scaled input), timed in a fresh random order within each sample, as the pages
+# time their candidate kernels; families run one after another, so that a small problem's samples
+# do not start from caches another, unrelated problem has just swept.
+PER_CONFIG_FAMILIES = [["n129_d32_f16_causal"],
+                       ["n512_d64_f16_causal", "n512_d64_f16_noncausal", "n512_d64_f16_causal_qx30"],
+                       ["b4_h16_n4096_d128_bf16", "b4_h16_n4096_d128_bf16_bnhd"],
+                       ["gqa_b2_h32x8_n8192_d128_bf16"], ["varlen16_h16_d128_bf16"], ["chunk2048_cache16384_gqa"],
+                       ["window4096_n16384", "global64_window4096_n16384"], ["decode_b8_h32x8_k32768"],
+                       ["bwd_b4_h16_n4096_d128_bf16", "bwd_gqa_b2_h32x8_n8192_d128_bf16"]]
+PER_CONFIG = [n for fam in PER_CONFIG_FAMILIES for n in fam]
 
 
 def parse_args():
@@ -523,80 +529,83 @@ def per_config_report(stream, device, peaks, pool, gated=None, samples=7, calls=
     """Page-style timing of every workload: a correctness gate first; 5
     warm-up calls; 7 samples of 20 calls each, per call the median (with min,
     max and every raw sample kept), CUDA events and CUDA-graph replay as
-    separate experiments.  Every workload stays resident, and within each
-    sample the workloads run in a fresh random order (recorded)."""
+    separate experiments.  Within each sample the workloads of one family
+    (PER_CONFIG_FAMILIES) run in a fresh random order (seeded, recorded)."""
     from exact_tiled_attention_19_gb300 import workloads as W
     import torch
     gated = gated or {}
-    out, live = {}, {}
-    for name in PER_CONFIG:
-        w = W.WORKLOADS[name]
-        inp, dev = device_inputs(w, device)
-        call = make_call(w, dev, stream)
-        with torch.cuda.stream(stream):
-            call()
-        torch.cuda.synchronize()
-        ok, err, err_lse = gated[name] if name in gated else correctness_gate(w, inp, dev, pool)
-        entry = {"gate": "pass" if ok else "FAIL"}
-        if w.backward:
-            entry["gate_error_to_bound_ratio"] = err
-        else:
-            entry["gate_max_abs_dO"] = err
-            entry["gate_max_abs_dlse"] = err_lse
-        out[name] = entry
-        del inp
-        if ok:
-            live[name] = (w, dev, call)
-    graphs, ev, gr = {}, {n: [] for n in live}, {n: [] for n in live}
-    with torch.cuda.stream(stream):
-        for name, (w, dev, call) in live.items():
-            for _ in range(warm):
+    rng = np.random.default_rng(seed)
+    out, orders = {}, {}
+    for fam in PER_CONFIG_FAMILIES:
+        live = {}
+        for name in fam:
+            w = W.WORKLOADS[name]
+            inp, dev = device_inputs(w, device)
+            call = make_call(w, dev, stream)
+            with torch.cuda.stream(stream):
                 call()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(calls):
+            torch.cuda.synchronize()
+            ok, err, err_lse = gated[name] if name in gated else correctness_gate(w, inp, dev, pool)
+            entry = {"gate": "pass" if ok else "FAIL"}
+            if w.backward:
+                entry["gate_error_to_bound_ratio"] = err
+            else:
+                entry["gate_max_abs_dO"] = err
+                entry["gate_max_abs_dlse"] = err_lse
+            out[name] = entry
+            del inp
+            if ok:
+                live[name] = (w, dev, call)
+        graphs, ev, gr = {}, {n: [] for n in live}, {n: [] for n in live}
+        with torch.cuda.stream(stream):
+            for name, (w, dev, call) in live.items():
+                for _ in range(warm):
                     call()
-            g.replay()
-            graphs[name] = g
-        torch.cuda.synchronize()
-        rng = np.random.default_rng(seed)
-        orders = []
-        for _ in range(samples):
-            order = [str(n) for n in rng.permutation(list(live))]
-            orders.append(order)
-            for name in order:
-                call = live[name][2]
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                for _ in range(calls):
-                    call()
-                b.record(stream)
-                b.synchronize()
-                ev[name].append(a.elapsed_time(b) * 1e3 / calls)
-                a.record(stream)
-                graphs[name].replay()
-                b.record(stream)
-                b.synchronize()
-                gr[name].append(a.elapsed_time(b) * 1e3 / calls)
-    for name, (w, dev, call) in live.items():
-        e, g = ev[name], gr[name]
-        entry = out[name]
-        entry.update({"us_event_median": round(statistics.median(e), 3), "us_event_min": round(min(e), 3),
-                      "us_event_max": round(max(e), 3), "us_graph_median": round(statistics.median(g), 3),
-                      "us_graph_min": round(min(g), 3), "us_graph_max": round(max(g), 3),
-                      "us_event_samples": [round(x, 3) for x in e], "us_graph_samples": [round(x, 3) for x in g]})
-        us = entry["us_graph_median"]
-        tf = w.flops() / (us * 1e-6) / 1e12
-        entry["tflops_graph"] = round(tf, 2)
-        entry["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
-        entry["achieved_gbs_graph"] = round(w.io_bytes() / (us * 1e-6) / 1e9, 1)
-        entry["frac_of_hbm"] = round(entry["achieved_gbs_graph"] / peaks["hbm_gbs"], 4)
-        if w.splitkv:
-            entry["num_splits"] = dev["splits"]
-    del graphs, live
-    torch.cuda.empty_cache()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(calls):
+                        call()
+                g.replay()
+                graphs[name] = g
+            torch.cuda.synchronize()
+            fam_orders = []
+            for _ in range(samples):
+                order = [str(n) for n in rng.permutation(list(live))]
+                fam_orders.append(order)
+                for name in order:
+                    call = live[name][2]
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(calls):
+                        call()
+                    b.record(stream)
+                    b.synchronize()
+                    ev[name].append(a.elapsed_time(b) * 1e3 / calls)
+                    a.record(stream)
+                    graphs[name].replay()
+                    b.record(stream)
+                    b.synchronize()
+                    gr[name].append(a.elapsed_time(b) * 1e3 / calls)
+            orders[" / ".join(fam)] = fam_orders
+        for name, (w, dev, call) in live.items():
+            e, g = ev[name], gr[name]
+            entry = out[name]
+            entry.update({"us_event_median": round(statistics.median(e), 3), "us_event_min": round(min(e), 3),
+                          "us_event_max": round(max(e), 3), "us_graph_median": round(statistics.median(g), 3),
+                          "us_graph_min": round(min(g), 3), "us_graph_max": round(max(g), 3),
+                          "us_event_samples": [round(x, 3) for x in e], "us_graph_samples": [round(x, 3) for x in g]})
+            us = entry["us_graph_median"]
+            tf = w.flops() / (us * 1e-6) / 1e12
+            entry["tflops_graph"] = round(tf, 2)
+            entry["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
+            entry["achieved_gbs_graph"] = round(w.io_bytes() / (us * 1e-6) / 1e9, 1)
+            entry["frac_of_hbm"] = round(entry["achieved_gbs_graph"] / peaks["hbm_gbs"], 4)
+            if w.splitkv:
+                entry["num_splits"] = dev["splits"]
+        del graphs, live
+        torch.cuda.empty_cache()
     meta = {"samples": samples, "calls_per_sample": calls, "warmup_calls": warm, "order_seed": seed,
-            "variant_order_per_sample": orders}
+            "families": PER_CONFIG_FAMILIES, "variant_order_per_sample": orders}
     return out, meta
 
 
