@@ -38,10 +38,15 @@
 //                    takes the place of its dO tile once dV has read it.
 //   warp 13          tensor-memory allocation and MMA issue (one thread).
 //
-// Tensor memory (512 columns): dK [0, D), dV [128, 128 + D), S^T [256, 384)
-// (P^T of query columns [64c, 64c + 64) packed into [256 + 64c, 256 + 64c +
-// 32); dQ_i over [256, 256 + D) once dV has read P^T), dP^T [384, 512) (dS^T
-// packed likewise at 384 + 64c).
+// Tensor memory (512 columns): dK [0, D), dV [128, 128 + D), and two
+// 128-column regions R0 = [256, 384), R1 = [384, 512) that swap roles every
+// step: step i forms S^T in R(i mod 2) (P^T of query columns [64c, 64c + 64)
+// packed into its first 32 columns of each half; dQ_i over it once dV has
+// read P^T) and dP^T in the other region (dS^T packed likewise).  The next
+// step's S^T goes into the region of this step's dS^T, which the dK product
+// has consumed by then (the same thread issued it first), so it need not
+// wait for dQ_i to be read out: the read-out overlaps the next step's P, and
+// only the next dP^T, which overwrites dQ_i, waits for it.
 #pragma once
 
 #include <cstdint>
@@ -90,7 +95,10 @@ struct BwdCfg {
   static constexpr int OFF_NSD = OFF_LSE + 2 * 512;        // two stages of 128 floats
   static constexpr int SMEM_BYTES = OFF_NSD + 2 * 512 + 1024;
   static constexpr uint32_t SBO = 8 * SW_BYTES;
-  static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384, TMEM_COLS = 512;
+  static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_R0 = 256, TMEM_COLS = 512;
+  // Regions of step i: S^T (then dQ_i) and dP^T (then dS^T).
+  static constexpr uint32_t tm_s(int i) { return TM_R0 + (uint32_t)(i & 1) * 128; }
+  static constexpr uint32_t tm_dp(int i) { return TM_R0 + (uint32_t)((i + 1) & 1) * 128; }
   static constexpr int THREADS = 512;
   static constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
   // Register split: 512 threads launch with 128 registers each; the dQ
@@ -201,7 +209,7 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
   const uint64_t ds_mn0 = smem_desc(smem_u32(smem + C::ds_offset(0)), 128 * 128, 1024, kSw128);
   const uint64_t ds_mn1 = smem_desc(smem_u32(smem + C::ds_offset(1)), 128 * 128, 1024, kSw128);
   const uint64_t slot_step = (uint64_t)(C::TILE >> 4);
-  const uint32_t tDK = tmem + C::TM_DK, tDV = tmem + C::TM_DV, tS = tmem + C::TM_S, tDP = tmem + C::TM_DP;
+  const uint32_t tDK = tmem + C::TM_DK, tDV = tmem + C::TM_DV;
 
   if (!mbar_wait(&sb.kv_full, 0, status)) return;
   for (int i = 0; i < u.steps; ++i) {
@@ -209,8 +217,8 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
     const uint64_t q_k = q_kmaj + slot * slot_step, q_m = q_mn + slot * slot_step;
     const uint64_t do_k = do_kmaj + slot * slot_step, do_m = do_mn + slot * slot_step;
     const uint64_t ds_mn = slot ? ds_mn1 : ds_mn0;
+    const uint32_t tS = tmem + C::tm_s(i), tDP = tmem + C::tm_dp(i);
     if (!mbar_wait(&sb.q_full[slot], (i >> 1) & 1, status)) return;
-    if (i > 0 && !mbar_wait(&sb.dq_empty, (i - 1) & 1, status)) return;
     tc_fence_after();
     // S^T = K Q^T over d in 16-element steps.
 #pragma unroll
@@ -220,7 +228,9 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
       mma_ss(tS, k_kmaj + off, q_k + off, id_s, kk > 0 ? 1u : 0u);
     }
     mma_commit(&sb.s_full);
+    // dP^T overwrites dQ_(i-1) (same region): it waits for the read-out.
     if (!mbar_wait(&sb.do_full[slot], (i >> 1) & 1, status)) return;
+    if (i > 0 && !mbar_wait(&sb.dq_empty, (i - 1) & 1, status)) return;
     tc_fence_after();
     // dP^T = V dO^T.
 #pragma unroll
@@ -292,7 +302,6 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
   constexpr uint32_t FULL = 0xffffffffu;
   const int t = threadIdx.x & 127;
   const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
-  const uint32_t tS = tmem + C::TM_S + lane_off + 64 * half, tDP = tmem + C::TM_DP + lane_off + 64 * half;
   const int key = u.kb0 + t;
   // Query rows that may read this key: c - win_left <= key <= c + win_right
   // with c = q + Nk - Nq, i.e. q in [key - delta - win_right, key - delta + win_left].
@@ -306,6 +315,7 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
 
   for (int i = 0; i < u.steps; ++i) {
     const int q0 = u.q0(i) + 64 * half, slot = i & 1;
+    const uint32_t tS = tmem + C::tm_s(i) + lane_off + 64 * half, tDP = tmem + C::tm_dp(i) + lane_off + 64 * half;
     const int64_t lo_rel = qlo - q0, hi_rel = qhi - q0;
     const int lim_lo = lo_rel < -1 ? -1 : (int)lo_rel, lim_hi = hi_rel > 64 ? 64 : (int)hi_rel;
     const bool warp_masked = __any_sync(FULL, lim_lo > 0 || lim_hi < 63);
@@ -431,7 +441,7 @@ __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t 
   using C = BwdCfg<D>;
   const int t = threadIdx.x & 127;
   const bool leader = t == 0;
-  const uint32_t tS = tmem + C::TM_S + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16);
+  const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
   uint8_t* stage_row = smem + C::OFF_STAGE + t * 128;
   int box = 0;  // boxes staged so far: the phase of stage_free / stage_full
   bool ok = true;
@@ -439,6 +449,7 @@ __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t 
   for (int i = 0; i < u.steps && ok; ++i) {
     if (!bwd_warp_wait(&sb.dq_full, i & 1, p.status)) break;
     tc_fence_after();
+    const uint32_t tS = tmem + C::tm_s(i) + lane_off;
     uint32_t r[D];
 #pragma unroll
     for (int c = 0; c < D; c += 32) tmem_ld_x32(tS + c, r + c);
