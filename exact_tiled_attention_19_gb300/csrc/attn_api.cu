@@ -316,14 +316,14 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
 bool head_dim_ok(int D) { return D == 32 || D == 64 || D == 128; }
 
 // 3-D FP32 map over the backward's dQ buffer [rows_bh = B * Hq][Nq][D] for
-// TMA reduce-adds of (32 columns x 128 rows) boxes, 128-byte swizzled; rows
+// TMA reduce-adds of (32 columns x 32 rows) boxes, 128-byte swizzled; rows
 // past Nq of a (batch, head) fall outside the map.
 int encode_dq_map(CUtensorMap* map, float* dq_acc, int D, int64_t Nq, int64_t rows_bh) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return fail_cuda(cudaErrorNotSupported);
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Nq, (cuuint64_t)rows_bh};
   cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)Nq * D * 4};
-  cuuint32_t box[3] = {32u, 128u, 1u};
+  cuuint32_t box[3] = {32u, 32u, 1u};
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dq_acc, dims, strides, box, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

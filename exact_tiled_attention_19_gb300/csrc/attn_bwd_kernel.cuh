@@ -31,8 +31,9 @@
 //                    dS^T from dP^T (into tensor memory and, transposed, into
 //                    shared memory for dQ).  Epilogue: dK (0) and dV (1).
 //   warpgroup 2      thread t owns query row t of dQ_i: reads it from tensor
-//                    memory, stages it in shared memory 32 columns at a time,
-//                    and one thread adds each staged box to the FP32 buffer.
+//                    memory; each warp stages its 32 rows in shared memory
+//                    32 columns at a time and its lane 0 adds each staged box
+//                    to the FP32 buffer, the four warps independently.
 //   warp 12          TMA: K and V once; per step Q with its lse and dO with
 //                    its D, two stages each.  At D = 128 the dS tile of a step
 //                    takes the place of its dO tile once dV has read it.
@@ -89,8 +90,9 @@ struct BwdCfg {
   static constexpr int DS_BYTES = 128 * 128 * 2;       // dS, 128 queries x 128 keys, MN-major, 128B swizzle
   static constexpr bool DS_IN_DO = TILE == DS_BYTES;   // D = 128: dS of a step over its dO stage
   static constexpr int OFF_DS = 6 * TILE;              // otherwise a tile of its own
-  static constexpr int OFF_STAGE = OFF_DS + (DS_IN_DO ? 0 : DS_BYTES);  // dQ staging: 128 rows x 32 FP32
-  static constexpr int STAGE_BYTES = 128 * 128;
+  // dQ staging: one box of 32 rows x 32 FP32 (4 KB) per warp of the dQ warpgroup.
+  static constexpr int OFF_STAGE = OFF_DS + (DS_IN_DO ? 0 : DS_BYTES);
+  static constexpr int STAGE_BYTES = 4 * 32 * 128;
   static constexpr int OFF_LSE = OFF_STAGE + STAGE_BYTES;  // two stages of 128 floats
   static constexpr int OFF_NSD = OFF_LSE + 2 * 512;        // two stages of 128 floats
   static constexpr int SMEM_BYTES = OFF_NSD + 2 * 512 + 1024;
@@ -123,8 +125,6 @@ struct BwdBarriers {
   uint64_t dq_full;                  // dQ_i in tensor memory (the step's dK and dQ products are done)
   uint64_t dq_empty;                 // dQ_i read out (128 arrivals)
   uint64_t kv_done;                  // last dK / dV product done
-  uint64_t stage_free;               // the dQ staging box may be written (leader, once per box)
-  uint64_t stage_full;               // the dQ staging box is written (128 arrivals per box)
   uint64_t fin;                      // every MMA the CTA issued has completed
   uint32_t tmem_base;
 };
@@ -430,23 +430,22 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
 }
 
 // Warpgroup 2: thread t owns query row q0 + t of each step's dQ contribution.
-// The row is read from tensor memory (which frees it for the next step),
-// then staged 32 columns at a time in a swizzled shared-memory box that one
-// thread adds to the FP32 dQ buffer with a TMA reduce (rows past Nq fall
-// outside the map and are dropped).  The box is handed back and forth on two
-// mbarriers, so every wait is bounded.
+// The row is read from tensor memory (which frees it for the next step).
+// Each warp then stages its 32 rows, 32 columns at a time, in a swizzled box
+// of its own, which its lane 0 adds to the FP32 dQ buffer with a TMA reduce
+// (rows past Nq fall outside the map and are dropped) after the warp's
+// previous box has left shared memory.  The four warps keep four reduces in
+// flight; one 128-row box handed between the warps on mbarriers kept one, and
+// the reduces' latency then set the step time.
 template <int D>
 __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t tmem, const BwdUnit u,
                                        const BwdParams& p, const CUtensorMap* tmDQ) {
   using C = BwdCfg<D>;
-  const int t = threadIdx.x & 127;
-  const bool leader = t == 0;
-  const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
-  uint8_t* stage_row = smem + C::OFF_STAGE + t * 128;
-  int box = 0;  // boxes staged so far: the phase of stage_free / stage_full
-  bool ok = true;
-  if (leader) mbar_arrive(&sb.stage_free);
-  for (int i = 0; i < u.steps && ok; ++i) {
+  const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  uint8_t* box_base = smem + C::OFF_STAGE + wq * 4096;
+  uint8_t* stage_row = box_base + lane * 128;
+  for (int i = 0; i < u.steps; ++i) {
     if (!bwd_warp_wait(&sb.dq_full, i & 1, p.status)) break;
     tc_fence_after();
     const uint32_t tS = tmem + C::tm_s(i) + lane_off;
@@ -460,30 +459,22 @@ __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t 
     mbar_arrive(&sb.dq_empty);
     const int h = u.head(i), q0 = u.q0(i);
 #pragma unroll
-    for (int c = 0; c < D && ok; c += 32, ++box) {
-      if (!bwd_warp_wait(&sb.stage_free, box & 1, p.status)) {
-        ok = false;
-        break;
-      }
+    for (int c = 0; c < D; c += 32) {
+      if (lane == 0) bulk_wait_read_all();  // the warp's previous box has left shared memory
+      __syncwarp();
 #pragma unroll
       for (int un = 0; un < 8; ++un)
-        *reinterpret_cast<uint4*>(stage_row + ((un ^ (t & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(stage_row + ((un ^ (lane & 7)) << 4)) =
             make_uint4(r[c + 4 * un], r[c + 4 * un + 1], r[c + 4 * un + 2], r[c + 4 * un + 3]);
       fence_proxy_async_smem();
-      mbar_arrive(&sb.stage_full);
-      if (leader) {
-        if (!mbar_wait(&sb.stage_full, box & 1, p.status)) {
-          ok = false;  // the other threads leave at their next bounded wait
-          break;
-        }
-        tma_reduce_add_3d(tmDQ, smem + C::OFF_STAGE, c, q0, u.b * p.Hq + h);
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(tmDQ, box_base, c, q0 + 32 * wq, u.b * p.Hq + h);
         bulk_commit_group();
-        bulk_wait_read_all();  // the box has left shared memory
-        mbar_arrive(&sb.stage_free);
       }
     }
   }
-  if (leader) bulk_wait_all();
+  if (lane == 0) bulk_wait_all();
 }
 
 // Grid: x = key block, y = key/value head, z = batch.
@@ -530,8 +521,6 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&sb.dq_full, 1);
     mbar_init(&sb.dq_empty, 128);
     mbar_init(&sb.kv_done, 1);
-    mbar_init(&sb.stage_free, 1);
-    mbar_init(&sb.stage_full, 128);
     mbar_init(&sb.fin, 1);
     fence_mbar_init();
   }
