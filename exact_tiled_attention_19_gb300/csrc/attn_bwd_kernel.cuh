@@ -46,8 +46,9 @@
 // read P^T) and dP^T in the other region (dS^T packed likewise).  The next
 // step's S^T goes into the region of this step's dS^T, which the dK product
 // has consumed by then (the same thread issued it first), so it need not
-// wait for dQ_i to be read out: the read-out overlaps the next step's P, and
-// only the next dP^T, which overwrites dQ_i, waits for it.
+// wait for dQ_i to be read out; it is issued between dK_i and dQ_i, so that
+// the next P phase starts while dQ_i is formed and read out.  Only the next
+// dP^T, which overwrites dQ_i, waits for the read-out.
 #pragma once
 
 #include <cstdint>
@@ -211,16 +212,13 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
   const uint64_t slot_step = (uint64_t)(C::TILE >> 4);
   const uint32_t tDK = tmem + C::TM_DK, tDV = tmem + C::TM_DV;
 
-  if (!mbar_wait(&sb.kv_full, 0, status)) return;
-  for (int i = 0; i < u.steps; ++i) {
+  // S^T of step i into its region (K-major Q of the step's stage).
+  auto issue_s = [&](int i) -> bool {
     const int slot = i & 1;
-    const uint64_t q_k = q_kmaj + slot * slot_step, q_m = q_mn + slot * slot_step;
-    const uint64_t do_k = do_kmaj + slot * slot_step, do_m = do_mn + slot * slot_step;
-    const uint64_t ds_mn = slot ? ds_mn1 : ds_mn0;
-    const uint32_t tS = tmem + C::tm_s(i), tDP = tmem + C::tm_dp(i);
-    if (!mbar_wait(&sb.q_full[slot], (i >> 1) & 1, status)) return;
+    if (!mbar_wait(&sb.q_full[slot], (i >> 1) & 1, status)) return false;
     tc_fence_after();
-    // S^T = K Q^T over d in 16-element steps.
+    const uint64_t q_k = q_kmaj + slot * slot_step;
+    const uint32_t tS = tmem + C::tm_s(i);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint64_t off =
@@ -228,6 +226,16 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
       mma_ss(tS, k_kmaj + off, q_k + off, id_s, kk > 0 ? 1u : 0u);
     }
     mma_commit(&sb.s_full);
+    return true;
+  };
+  if (!mbar_wait(&sb.kv_full, 0, status)) return;
+  if (!issue_s(0)) return;
+  for (int i = 0; i < u.steps; ++i) {
+    const int slot = i & 1;
+    const uint64_t q_m = q_mn + slot * slot_step;
+    const uint64_t do_k = do_kmaj + slot * slot_step, do_m = do_mn + slot * slot_step;
+    const uint64_t ds_mn = slot ? ds_mn1 : ds_mn0;
+    const uint32_t tS = tmem + C::tm_s(i), tDP = tmem + C::tm_dp(i);
     // dP^T overwrites dQ_(i-1) (same region): it waits for the read-out.
     if (!mbar_wait(&sb.do_full[slot], (i >> 1) & 1, status)) return;
     if (i > 0 && !mbar_wait(&sb.dq_empty, (i - 1) & 1, status)) return;
@@ -248,13 +256,16 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
       mma_ts(tDV, tS + C::packed_col(kk), do_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv,
              (i > 0 || kk > 0) ? 1u : 0u);
     mma_commit(&sb.dv_done);
-    // dK += dS^T Q, then dQ_i = dS K (over the 128 keys) into the S^T columns.
+    // dK += dS^T Q; then the next step's S^T, which goes over this step's
+    // dS^T (read by the dK product just issued), so that the next P phase
+    // does not wait behind dQ_i; then dQ_i = dS K into this step's S^T columns.
     if (!mbar_wait(&sb.ds_ready, i & 1, status)) return;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ts(tDK, tDP + C::packed_col(kk), q_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv,
              (i > 0 || kk > 0) ? 1u : 0u);
+    if (i + 1 < u.steps && !issue_s(i + 1)) return;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ss(tS, ds_mn + (uint64_t)((kk * 16 * 128) >> 4), k_mn + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_q,
