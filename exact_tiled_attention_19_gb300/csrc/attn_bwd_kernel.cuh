@@ -39,16 +39,14 @@
 //                    takes the place of its dO tile once dV has read it.
 //   warp 13          tensor-memory allocation and MMA issue (one thread).
 //
-// Tensor memory (512 columns): dK [0, D), dV [128, 128 + D), and two
-// 128-column regions R0 = [256, 384), R1 = [384, 512) that swap roles every
-// step: step i forms S^T in R(i mod 2) (P^T of query columns [64c, 64c + 64)
-// packed into its first 32 columns of each half; dQ_i over it once dV has
-// read P^T) and dP^T in the other region (dS^T packed likewise).  The next
-// step's S^T goes into the region of this step's dS^T, which the dK product
-// has consumed by then (the same thread issued it first), so it need not
-// wait for dQ_i to be read out; it is issued between dK_i and dQ_i, so that
-// the next P phase starts while dQ_i is formed and read out.  Only the next
-// dP^T, which overwrites dQ_i, waits for the read-out.
+// Tensor memory (512 columns): dK [0, D), dV [128, 128 + D), S^T [256, 384)
+// (P^T of query columns [64c, 64c + 64) packed into [256 + 64c, 256 + 64c +
+// 32)), dP^T [384, 512) (dS^T packed likewise at 384 + 64c; dQ_i over it once
+// dK has read dS^T).  The dS phase reads P^T back first, so the next step's
+// S^T is issued right after dV_i and that step's P phase finds its scores
+// ready as soon as this dS phase ends; only the next dP^T, which overwrites
+// dQ_i, waits for the dQ read-out.  Per step the tensor core runs
+// dP_i, dV_i, S_(i+1), dK_i, dQ_i.
 #pragma once
 
 #include <cstdint>
@@ -98,10 +96,7 @@ struct BwdCfg {
   static constexpr int OFF_NSD = OFF_LSE + 2 * 512;        // two stages of 128 floats
   static constexpr int SMEM_BYTES = OFF_NSD + 2 * 512 + 1024;
   static constexpr uint32_t SBO = 8 * SW_BYTES;
-  static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_R0 = 256, TMEM_COLS = 512;
-  // Regions of step i: S^T (then dQ_i) and dP^T (then dS^T).
-  static constexpr uint32_t tm_s(int i) { return TM_R0 + (uint32_t)(i & 1) * 128; }
-  static constexpr uint32_t tm_dp(int i) { return TM_R0 + (uint32_t)((i + 1) & 1) * 128; }
+  static constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384, TMEM_COLS = 512;
   static constexpr int THREADS = 512;
   static constexpr int PRODUCER_WARP = 12, MMA_WARP = 13;
   // Register split: 512 threads launch with 128 registers each; the dQ
@@ -123,6 +118,7 @@ struct BwdBarriers {
   uint64_t dv_done;                  // dV_i is done (dO_i read by the tensor core for the last time)
   uint64_t s_full, dp_full;          // S^T / dP^T of the step are in tensor memory
   uint64_t p_ready, ds_ready;        // P^T / dS^T (and dS in shared memory) written (256 arrivals)
+  uint64_t p_read;                   // P^T read back by the dS phase (256 arrivals)
   uint64_t dq_full;                  // dQ_i in tensor memory (the step's dK and dQ products are done)
   uint64_t dq_empty;                 // dQ_i read out (128 arrivals)
   uint64_t kv_done;                  // last dK / dV product done
@@ -210,7 +206,7 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
   const uint64_t ds_mn0 = smem_desc(smem_u32(smem + C::ds_offset(0)), 128 * 128, 1024, kSw128);
   const uint64_t ds_mn1 = smem_desc(smem_u32(smem + C::ds_offset(1)), 128 * 128, 1024, kSw128);
   const uint64_t slot_step = (uint64_t)(C::TILE >> 4);
-  const uint32_t tDK = tmem + C::TM_DK, tDV = tmem + C::TM_DV;
+  const uint32_t tDK = tmem + C::TM_DK, tDV = tmem + C::TM_DV, tS = tmem + C::TM_S, tDP = tmem + C::TM_DP;
 
   // S^T of step i into its region (K-major Q of the step's stage).
   auto issue_s = [&](int i) -> bool {
@@ -218,7 +214,6 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
     if (!mbar_wait(&sb.q_full[slot], (i >> 1) & 1, status)) return false;
     tc_fence_after();
     const uint64_t q_k = q_kmaj + slot * slot_step;
-    const uint32_t tS = tmem + C::tm_s(i);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint64_t off =
@@ -235,7 +230,6 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
     const uint64_t q_m = q_mn + slot * slot_step;
     const uint64_t do_k = do_kmaj + slot * slot_step, do_m = do_mn + slot * slot_step;
     const uint64_t ds_mn = slot ? ds_mn1 : ds_mn0;
-    const uint32_t tS = tmem + C::tm_s(i), tDP = tmem + C::tm_dp(i);
     // dP^T overwrites dQ_(i-1) (same region): it waits for the read-out.
     if (!mbar_wait(&sb.do_full[slot], (i >> 1) & 1, status)) return;
     if (i > 0 && !mbar_wait(&sb.dq_empty, (i - 1) & 1, status)) return;
@@ -256,19 +250,22 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
       mma_ts(tDV, tS + C::packed_col(kk), do_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv,
              (i > 0 || kk > 0) ? 1u : 0u);
     mma_commit(&sb.dv_done);
-    // dK += dS^T Q; then the next step's S^T, which goes over this step's
-    // dS^T (read by the dK product just issued), so that the next P phase
-    // does not wait behind dQ_i; then dQ_i = dS K into this step's S^T columns.
+    // The next step's S^T over P^T_i, once dV_i (issued above) and the dS
+    // phase have read it.
+    if (i + 1 < u.steps) {
+      if (!mbar_wait(&sb.p_read, i & 1, status)) return;
+      if (!issue_s(i + 1)) return;
+    }
+    // dK += dS^T Q, then dQ_i = dS K over dS^T (read by the dK product just issued).
     if (!mbar_wait(&sb.ds_ready, i & 1, status)) return;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ts(tDK, tDP + C::packed_col(kk), q_m + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_kv,
              (i > 0 || kk > 0) ? 1u : 0u);
-    if (i + 1 < u.steps && !issue_s(i + 1)) return;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ss(tS, ds_mn + (uint64_t)((kk * 16 * 128) >> 4), k_mn + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_q,
+      mma_ss(tDP, ds_mn + (uint64_t)((kk * 16 * 128) >> 4), k_mn + (uint64_t)((kk * 16 * C::SW_BYTES) >> 4), id_q,
              kk > 0 ? 1u : 0u);
     mma_commit(&sb.dq_full);
     mma_commit(&sb.q_empty[slot]);
@@ -313,6 +310,7 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
   constexpr uint32_t FULL = 0xffffffffu;
   const int t = threadIdx.x & 127;
   const uint32_t lane_off = (uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = tmem + C::TM_S + lane_off + 64 * half, tDP = tmem + C::TM_DP + lane_off + 64 * half;
   const int key = u.kb0 + t;
   // Query rows that may read this key: c - win_left <= key <= c + win_right
   // with c = q + Nk - Nq, i.e. q in [key - delta - win_right, key - delta + win_left].
@@ -326,7 +324,6 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
 
   for (int i = 0; i < u.steps; ++i) {
     const int q0 = u.q0(i) + 64 * half, slot = i & 1;
-    const uint32_t tS = tmem + C::tm_s(i) + lane_off + 64 * half, tDP = tmem + C::tm_dp(i) + lane_off + 64 * half;
     const int64_t lo_rel = qlo - q0, hi_rel = qhi - q0;
     const int lim_lo = lo_rel < -1 ? -1 : (int)lo_rel, lim_hi = hi_rel > 64 ? 64 : (int)hi_rel;
     const bool warp_masked = __any_sync(FULL, lim_lo > 0 || lim_hi < 63);
@@ -368,19 +365,26 @@ __device__ __forceinline__ void bwd_compute(BwdBarriers& sb, uint8_t* smem, uint
     if (!bwd_warp_wait(&sb.dp_full, i & 1, status)) return;
     tc_fence_after();
     uint8_t* ds_row = smem + C::ds_offset(slot) + half * (128 * 128) + t * 128;
+    // P^T of both chunks, read first so that the next S^T may overwrite it.
+    uint32_t pk[32], dr[32];
+    tmem_ld_x32(tS, pk);
+    tmem_ld_x32(tDP, dr);
+    tmem_ld_wait32(pk);
+    fence_regs32(dr);
+    tc_fence_before();
+    mbar_arrive(&sb.p_read);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
-      uint32_t dr[32], pk[16];
-      tmem_ld_x32(tDP + 32 * ch, dr);
-      tmem_ld_x16(tS + 16 * ch, pk);
-      tmem_ld_wait32(dr);  // waits for both loads
-      fence_regs16(pk);
+      if (ch == 1) {
+        tmem_ld_x32(tDP + 32, dr);
+        tmem_ld_wait32(dr);
+      }
       uint32_t ds[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const float2 nd = nsd[(32 * ch + j) / 2];
         float p0, p1, g0, g1;
-        bwd_unpack<BF16>(pk[j / 2], p0, p1);
+        bwd_unpack<BF16>(pk[16 * ch + j / 2], p0, p1);
         fma2(g0, g1, __uint_as_float(dr[j]), __uint_as_float(dr[j + 1]), scale, scale, nd.x, nd.y);
         fma2(g0, g1, p0, p1, g0, g1, 0.f, 0.f);
         ds[j / 2] = bwd_pack<BF16>(g0, g1);
@@ -453,16 +457,15 @@ __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t 
                                        const BwdParams& p, const CUtensorMap* tmDQ) {
   using C = BwdCfg<D>;
   const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
-  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  const uint32_t tDQ = tmem + C::TM_DP + ((uint32_t)(wq * 32) << 16);  // dQ_i lies over dP^T
   uint8_t* box_base = smem + C::OFF_STAGE + wq * 4096;
   uint8_t* stage_row = box_base + lane * 128;
   for (int i = 0; i < u.steps; ++i) {
     if (!bwd_warp_wait(&sb.dq_full, i & 1, p.status)) break;
     tc_fence_after();
-    const uint32_t tS = tmem + C::tm_s(i) + lane_off;
     uint32_t r[D];
 #pragma unroll
-    for (int c = 0; c < D; c += 32) tmem_ld_x32(tS + c, r + c);
+    for (int c = 0; c < D; c += 32) tmem_ld_x32(tDQ + c, r + c);
     tmem_ld_wait32(r);
 #pragma unroll
     for (int c = 32; c < D; c += 32) fence_regs32(r + c);
@@ -529,6 +532,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(&sb.dp_full, 1);
     mbar_init(&sb.p_ready, 256);
     mbar_init(&sb.ds_ready, 256);
+    mbar_init(&sb.p_read, 256);
     mbar_init(&sb.dq_full, 1);
     mbar_init(&sb.dq_empty, 128);
     mbar_init(&sb.kv_done, 1);
