@@ -279,6 +279,10 @@ __device__ __forceinline__ void bwd_mma(BwdBarriers& sb, uint8_t* smem, uint32_t
 }
 
 __device__ __forceinline__ bool bwd_warp_wait(uint64_t* bar, uint32_t parity, int* status) {
+  // Fast path: every lane probes once, and a phase that has already
+  // completed (the common case) costs one probe and a vote.  Otherwise lane 0
+  // waits (bounded) and hands the outcome to the warp.
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;

@@ -593,9 +593,14 @@ __device__ __forceinline__ void mma_role(SmemBarriers& sb, uint8_t* smem, uint32
 }
 
 // ----------------------------------------------------------------- softmax / correction / epilogue
-// Warp-wide wait: lane 0 polls the barrier and the outcome is broadcast, so
-// one thread per warp (not 32) touches the barrier word.
+// Warp-wide wait: while the phase is still open, lane 0 alone polls the
+// barrier and the outcome is broadcast, so one thread per warp (not 32)
+// keeps touching the barrier word.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status) {
+  // Fast path: every lane probes once, and a phase that has already
+  // completed (the common case) costs one probe and a vote.  Otherwise lane 0
+  // waits (bounded) and hands the outcome to the warp.
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
