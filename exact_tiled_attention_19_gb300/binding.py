@@ -8,6 +8,7 @@ The functions ``attn_fwd``, ``attn_fwd_ex``, ``attn_bwd``, ``attn_bwd_workspace_
 ``attn_fwd_varlen_splitkv_plan``,
 ``attn_fwd_varlen_global``,
 ``attn_fwd_varlen``, ``attn_fwd_varlen_ex``, ``attn_fwd_host``, ``attn_fwd_varlen_host``,
+``attn_fwd_varlen_host_plan``,
 ``etattn_status_string``, ``etattn_last_cuda_error``,
 ``etattn_read_device_status``, ``etattn_selftest_wait_timeout`` and
 ``etattn_version`` have the C names and
@@ -108,6 +109,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_host.restype = _int
         lib.attn_fwd_varlen_host.argtypes = [_vp] * 12 + [_int] * 8 + [ctypes.c_float, _vp]
         lib.attn_fwd_varlen_host.restype = _int
+        lib.attn_fwd_varlen_host_plan.argtypes = [_vp, _int, _int, ctypes.POINTER(ctypes.c_int32)]
+        lib.attn_fwd_varlen_host_plan.restype = _int
         lib.etattn_status_string.argtypes = [_int]
         lib.etattn_status_string.restype = ctypes.c_char_p
         lib.etattn_last_cuda_error.argtypes = []
@@ -225,6 +228,15 @@ def attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev,
     return lib.attn_fwd_host(q_host or None, k_host or None, v_host or None, o_host or None, lse_host or None,
                              q_dev or None, k_dev or None, v_dev or None, o_dev or None, lse_dev or None, B, Hq,
                              Hkv, N, D, dtype, causal, scale, stream or None)
+
+
+def attn_fwd_varlen_host_plan(cu_seqlens, max_chunks=8):
+    """C ``attn_fwd_varlen_host_plan`` on a host sequence of offsets: (status
+    or chunk count k, the k + 1 run bounds)."""
+    cu = (ctypes.c_int32 * max(len(cu_seqlens), 1))(*[int(x) for x in cu_seqlens])
+    bounds = (ctypes.c_int32 * 9)()
+    k = load_library().attn_fwd_varlen_host_plan(ctypes.addressof(cu), len(cu_seqlens) - 1, max_chunks, bounds)
+    return k, list(bounds[:k + 1]) if k > 0 else []
 
 
 def attn_fwd_varlen_host(q_host, k_host, v_host, o_host, lse_host, cu_seqlens_host, q_dev, k_dev, v_dev, o_dev,

@@ -268,12 +268,14 @@ bool has_few_key_rows(int64_t Lq, int64_t Lk, int64_t wl, int64_t wr, int64_t wr
 // sub-tiles taking alternate key tiles.
 cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const FwdParams& p, int64_t tokens, unsigned gy, unsigned gz, int num_sms, bool general,
-                   bool few_keys, cudaStream_t s, int64_t key_tiles = 0) {
+                   bool few_keys, cudaStream_t s, int64_t key_tiles = 0, int ks_force = -1) {
   const bool bf = dtype == ETATTN_BF16;
   const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
   const int64_t blocks1 = (tokens + 127) / 128, blocks2 = (tokens + 255) / 256;
+  // ks_force >= 0: a chunk of a larger call takes the whole call's key-split
+  // choice (the split changes the order of the sum over key tiles).
   const bool ksplit = splits == 1 && p.qpack == 1 && p.num_global == 0 && key_tiles >= 2 &&
-                      2 * blocks1 * (int64_t)gy * gz <= num_sms;
+                      (ks_force >= 0 ? ks_force == 1 : 2 * blocks1 * (int64_t)gy * gz <= num_sms);
   // Up to 128 query rows fill one sub-tile: a second one would only idle.
   const int nsub = (p.qpack > 1 || tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
   const int64_t gx = (ksplit || nsub == 1 ? blocks1 : blocks2) * splits;
@@ -436,7 +438,8 @@ int window_right_of(int wr, int causal) {
 // Validates every argument; launches only when do_launch is set.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
              int Nk, int D, int dtype, const int64_t* strides, int causal, int window_left, int window_right,
-             float scale, void* stream, bool do_launch, const SplitArgs* split = nullptr, int num_global = 0) {
+             float scale, void* stream, bool do_launch, const SplitArgs* split = nullptr, int num_global = 0,
+             int ks_force = -1) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (B < 0 || Hq < 0 || Nq < 0 || Nk < 0 || !head_dim_ok(D)) return ETATTN_ERR_BAD_SHAPE;
   if (Nq > kMaxTokens || Nk > kMaxTokens || B > kMaxGridYZ || Hq > kMaxGridYZ) return ETATTN_ERR_BAD_SHAPE;
@@ -546,7 +549,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   const bool few = dtype == ETATTN_BF16 && has_few_key_rows(Nq, Nk, p.win_left, p.win_right, p.win_right_causal,
                                                             p.num_global);
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)Nq * qpack, (unsigned)(Hq / qpack), (unsigned)B, num_sms,
-                         general, few, st, (Nk + 127) / 128);
+                         general, few, st, (Nk + 127) / 128, ks_force);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splitting) {
     CombineParams c{};
@@ -745,8 +748,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
 
 // Host mirror of packed offsets: 0, non-decreasing, ending at total, every
 // length <= max_len.
-bool seqlens_ok(const int32_t* cu, int num_seqs, int total, int max_len) {
-  if (cu[0] != 0 || cu[num_seqs] != total) return false;
+// whole = false: the offsets of a run of sequences inside a packed batch
+// (they start at or after 0 and end at or before the total).
+bool seqlens_ok(const int32_t* cu, int num_seqs, int total, int max_len, bool whole = true) {
+  if (whole ? (cu[0] != 0 || cu[num_seqs] != total) : (cu[0] < 0 || cu[num_seqs] > total)) return false;
   for (int s = 0; s < num_seqs; ++s) {
     const int64_t len = (int64_t)cu[s + 1] - cu[s];
     if (len < 0 || len > max_len) return false;
@@ -758,7 +763,8 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
                 const int32_t* cu_seqlens_k, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_k_host,
                 int num_seqs, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int D,
                 int dtype, const int64_t* strides, int causal, int window_left, int window_right, float scale,
-                void* stream, bool do_launch, const SplitArgs* split = nullptr, int num_global = 0) {
+                void* stream, bool do_launch, const SplitArgs* split = nullptr, int num_global = 0,
+                bool sub_range = false, int ks_force = -1) {
   if (dtype != ETATTN_F16 && dtype != ETATTN_BF16) return ETATTN_ERR_BAD_DTYPE;
   if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0 || Hq < 0 ||
       !head_dim_ok(D))
@@ -770,9 +776,9 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
   if (strides == nullptr) return ETATTN_ERR_NULL_PTR;
   if (num_global < 0 || (num_global > 0 && split != nullptr)) return ETATTN_ERR_BAD_SHAPE;
   if (split != nullptr && (split->num_splits < 1 || split->num_splits > kMaxSplits)) return ETATTN_ERR_BAD_SHAPE;
-  if (cu_seqlens_q_host && !seqlens_ok(cu_seqlens_q_host, num_seqs, total_q, max_seqlen_q))
+  if (cu_seqlens_q_host && !seqlens_ok(cu_seqlens_q_host, num_seqs, total_q, max_seqlen_q, !sub_range))
     return ETATTN_ERR_BAD_SEQLENS;
-  if (cu_seqlens_k_host && !seqlens_ok(cu_seqlens_k_host, num_seqs, total_k, max_seqlen_k))
+  if (cu_seqlens_k_host && !seqlens_ok(cu_seqlens_k_host, num_seqs, total_k, max_seqlen_k, !sub_range))
     return ETATTN_ERR_BAD_SEQLENS;
   if (num_seqs == 0 || Hq == 0 || total_q == 0 || max_seqlen_q == 0) return ETATTN_OK;
   const bool has_keys = total_k > 0;
@@ -881,7 +887,7 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
                              p.win_right_causal, p.num_global);
   }
   cudaError_t e = launch(D, dtype, mq, mk, mv, p, (int64_t)max_seqlen_q * qpack, (unsigned)(Hq / qpack),
-                         (unsigned)num_seqs, num_sms, general, few, st, key_tiles);
+                         (unsigned)num_seqs, num_sms, general, few, st, key_tiles, ks_force);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splitting) {
     CombineParams c{};
@@ -902,6 +908,84 @@ int varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse
     if (e != cudaSuccess) return fail_cuda(e);
   }
   return ETATTN_OK;
+}
+
+// ---------------------------------------------------------------- host-buffer pipeline
+// The host-buffer calls cut the problem into chunks (whole sequences of a
+// packed batch, whole batches, or runs of KV heads) and pipeline them over
+// the current device's two copy streams: chunk c + 1's inputs travel to the
+// device while chunk c's kernel runs on the caller's stream, and chunk c's
+// outputs travel back meanwhile.  The streams and events are created on first
+// use and kept; a mutex per device orders the enqueues of concurrent calls.
+constexpr int kHostChunks = 8;
+
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in[kHostChunks] = {}, out[kHostChunks] = {};
+};
+HostPipe g_host_pipes[64];
+
+// Creates the device's copy streams and events once; the caller holds pipe.mu.
+int host_pipe_ready(HostPipe& hp) {
+  if (hp.ready) return ETATTN_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming);
+  for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+    e = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.out[c], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) return fail_cuda(e);
+  hp.ready = true;
+  return ETATTN_OK;
+}
+
+// Cuts n items with prefix sums pre[0..n] (pre[0] = 0 after rebasing) into at
+// most max_chunks runs of about equal weight: a run ends after the first item
+// whose prefix reaches the next multiple of total / chunks.  bounds[0..k] get
+// the item indices; returns k (0 when n == 0).
+int plan_runs(const int64_t* pre, int n, int max_chunks, int32_t* bounds) {
+  if (n <= 0) return 0;
+  const int k_max = std::max(1, std::min(std::min(max_chunks, kHostChunks), n));
+  const int64_t total = pre[n] - pre[0];
+  int k = 0;
+  bounds[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t done = pre[i + 1] - pre[0];
+    // close the run at item i when it reaches its share (the last run takes the rest)
+    if (i + 1 == n || (k + 1 < k_max && done * k_max >= (int64_t)(k + 1) * total && total > 0))
+      bounds[++k] = i + 1;
+  }
+  return k;
+}
+
+// The key-split choice `launch` makes for a whole square call of Hq heads
+// (one query row per head, no packing) over `seqs` sequences or batches of up
+// to `len` tokens, for its chunks to take.
+int key_split_of(int64_t len, int64_t Hq, int64_t seqs, int num_sms) {
+  const int64_t blocks1 = (len + 127) / 128;
+  return blocks1 >= 2 && 2 * blocks1 * Hq * seqs <= num_sms ? 1 : 0;
+}
+
+// Enqueues the start of a pipelined call: the copy streams wait for the work
+// already on the caller's stream.
+cudaError_t pipe_begin(HostPipe& hp, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(hp.start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.h2d, hp.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.start, 0);
+  return e;
+}
+
+// The caller's stream waits for the last output copy, so that the call's
+// completion is observed on it.
+cudaError_t pipe_end(HostPipe& hp, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(hp.end, hp.d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.end, 0);
+  return e;
 }
 
 }  // namespace
@@ -1055,6 +1139,17 @@ int attn_fwd_varlen_global(const void* q, const void* k, const void* v, void* o,
                      window_right, scale, stream, true, nullptr, window_is_everything ? 0 : num_global);
 }
 
+int attn_fwd_varlen_host_plan(const int32_t* cu_seqlens_host, int num_seqs, int max_chunks,
+                                         int32_t* seq_bounds) {
+  if (cu_seqlens_host == nullptr || seq_bounds == nullptr) return -ETATTN_ERR_NULL_PTR;
+  if (num_seqs < 0 || max_chunks < 1) return -ETATTN_ERR_BAD_SHAPE;
+  std::vector<int64_t> pre((size_t)num_seqs + 1);
+  for (int i = 0; i <= num_seqs; ++i) pre[i] = cu_seqlens_host[i];
+  for (int i = 0; i < num_seqs; ++i)
+    if (pre[i + 1] < pre[i]) return -ETATTN_ERR_BAD_SEQLENS;
+  return plan_runs(pre.data(), num_seqs, max_chunks, seq_bounds);
+}
+
 int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
                   void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int Hq, int Hkv, int N,
                   int D, int dtype, int causal, float scale, void* stream) {
@@ -1066,18 +1161,58 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
     return rc;
   if (B == 0 || Hq == 0 || N == 0) return ETATTN_OK;
   if (!q_host || !k_host || !v_host || !o_host) return ETATTN_ERR_NULL_PTR;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t nq = (size_t)B * Hq * N * D * 2, nkv = (size_t)B * Hkv * N * D * 2;
-  cudaError_t e = cudaMemcpyAsync(q_dev, q_host, nq, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(k_dev, k_host, nkv, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(v_dev, v_host, nkv, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  if (int rc = fwd_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, B, Hq, Hkv, N, N, D, dtype, st, causal, -1, -1, scale,
-                        stream, true))
-    return rc;
-  e = cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && lse_host)
-    e = cudaMemcpyAsync(lse_host, lse_dev, (size_t)B * Hq * N * sizeof(float), cudaMemcpyDeviceToHost, s);
+  // Chunks: runs of whole batches, or of KV heads (with their query heads)
+  // when there is one batch; each is contiguous in every buffer.
+  const int g = Hq / Hkv;
+  const bool by_batch = B > 1;
+  const int units = by_batch ? B : Hkv;
+  const int64_t q_unit = (by_batch ? (int64_t)Hq : g) * N * D * 2;  // bytes of one unit's Q (and O)
+  const int64_t kv_unit = (by_batch ? (int64_t)Hkv : 1) * N * D * 2;
+  const int64_t l_unit = (by_batch ? (int64_t)Hq : g) * N;          // lse entries of one unit
+  std::vector<int64_t> pre((size_t)units + 1);
+  for (int i = 0; i <= units; ++i) pre[i] = i;
+  int32_t bounds[kHostChunks + 1];
+  const int k = plan_runs(pre.data(), units, kHostChunks, bounds);
+  int dev = 0, num_sms = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status, &num_sms)) return rc;
+  const int ks = key_split_of(N, Hq, B, num_sms);
+  HostPipe& hp = g_host_pipes[dev];
+  std::lock_guard<std::mutex> lk(hp.mu);
+  if (int rc = host_pipe_ready(hp)) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto at = [](const void* base, int64_t off) { return static_cast<const char*>(base) + off; };
+  auto atw = [](void* base, int64_t off) { return static_cast<char*>(base) + off; };
+  cudaError_t e = pipe_begin(hp, s);
+  for (int c = 0; c < k && e == cudaSuccess; ++c) {
+    const int u0 = bounds[c], nu = bounds[c + 1] - bounds[c];
+    e = cudaMemcpyAsync(atw(q_dev, u0 * q_unit), at(q_host, u0 * q_unit), nu * q_unit, cudaMemcpyHostToDevice,
+                        hp.h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(atw(k_dev, u0 * kv_unit), at(k_host, u0 * kv_unit), nu * kv_unit, cudaMemcpyHostToDevice,
+                          hp.h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(atw(v_dev, u0 * kv_unit), at(v_host, u0 * kv_unit), nu * kv_unit, cudaMemcpyHostToDevice,
+                          hp.h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(hp.in[c], hp.h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in[c], 0);
+    if (e != cudaSuccess) break;
+    float* lse_c = lse_dev ? lse_dev + u0 * l_unit : nullptr;
+    if (int rc = fwd_impl(at(q_dev, u0 * q_unit), at(k_dev, u0 * kv_unit), at(v_dev, u0 * kv_unit),
+                          atw(o_dev, u0 * q_unit), lse_c, by_batch ? nu : 1, by_batch ? Hq : nu * g,
+                          by_batch ? Hkv : nu, N, N, D, dtype, st, causal, -1, -1, scale, stream, true, nullptr, 0,
+                          ks))
+      return rc;
+    e = cudaEventRecord(hp.out[c], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.out[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(atw(o_host, u0 * q_unit), at(o_dev, u0 * q_unit), nu * q_unit, cudaMemcpyDeviceToHost,
+                          hp.d2h);
+    if (e == cudaSuccess && lse_host)
+      e = cudaMemcpyAsync(lse_host + u0 * l_unit, lse_dev + u0 * l_unit, nu * l_unit * sizeof(float),
+                          cudaMemcpyDeviceToHost, hp.d2h);
+  }
+  if (e == cudaSuccess) e = pipe_end(hp, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }
@@ -1095,22 +1230,61 @@ int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_h
     return rc;
   if (num_seqs == 0 || Hq == 0 || total_tokens == 0 || max_seqlen == 0) return ETATTN_OK;
   if (!q_host || !k_host || !v_host || !o_host) return ETATTN_ERR_NULL_PTR;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t T = (size_t)total_tokens;
-  const size_t nq = T * Hq * D * 2, nkv = T * Hkv * D * 2;
-  cudaError_t e = cudaMemcpyAsync(cu_seqlens_dev, cu_seqlens_host, (size_t)(num_seqs + 1) * sizeof(int32_t),
-                                  cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(q_dev, q_host, nq, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(k_dev, k_host, nkv, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(v_dev, v_host, nkv, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev, cu_seqlens_dev, nullptr, nullptr,
-                           num_seqs, max_seqlen, max_seqlen, total_tokens, total_tokens, Hq, Hkv, D, dtype, st, causal,
-                           -1, -1, scale, stream, true))
-    return rc;
-  e = cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && lse_host)
-    e = cudaMemcpyAsync(lse_host, lse_dev, T * Hq * sizeof(float), cudaMemcpyDeviceToHost, s);
+  // Chunks: runs of whole sequences of about equal token counts; each chunk's
+  // rows are contiguous in Q, K, V and O and form one column band of lse
+  // [Hq, T].  A chunk's launch reads its own run of the offsets in place
+  // (absolute token positions inside the whole buffers).
+  const int64_t T = total_tokens;
+  const int64_t q_tok = (int64_t)Hq * D * 2, kv_tok = (int64_t)Hkv * D * 2;  // bytes per token
+  std::vector<int64_t> pre((size_t)num_seqs + 1);
+  for (int i = 0; i <= num_seqs; ++i) pre[i] = cu_seqlens_host[i];
+  int32_t bounds[kHostChunks + 1];
+  const int k = plan_runs(pre.data(), num_seqs, kHostChunks, bounds);
+  int dev = 0, num_sms = 0;
+  int* status = nullptr;
+  if (int rc = current_device(&dev, &status, &num_sms)) return rc;
+  const int ks = key_split_of(max_seqlen, Hq, num_seqs, num_sms);
+  HostPipe& hp = g_host_pipes[dev];
+  std::lock_guard<std::mutex> lk(hp.mu);
+  if (int rc = host_pipe_ready(hp)) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto at = [](const void* base, int64_t off) { return static_cast<const char*>(base) + off; };
+  auto atw = [](void* base, int64_t off) { return static_cast<char*>(base) + off; };
+  cudaError_t e = pipe_begin(hp, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(cu_seqlens_dev, cu_seqlens_host, (size_t)(num_seqs + 1) * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, hp.h2d);
+  for (int c = 0; c < k && e == cudaSuccess; ++c) {
+    const int a = bounds[c], b = bounds[c + 1];
+    const int64_t t0 = cu_seqlens_host[a], nt = (int64_t)cu_seqlens_host[b] - t0;
+    int len_max = 0;
+    for (int i = a; i < b; ++i) len_max = std::max(len_max, cu_seqlens_host[i + 1] - cu_seqlens_host[i]);
+    if (nt > 0) {
+      e = cudaMemcpyAsync(atw(q_dev, t0 * q_tok), at(q_host, t0 * q_tok), nt * q_tok, cudaMemcpyHostToDevice, hp.h2d);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(atw(k_dev, t0 * kv_tok), at(k_host, t0 * kv_tok), nt * kv_tok, cudaMemcpyHostToDevice,
+                            hp.h2d);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(atw(v_dev, t0 * kv_tok), at(v_host, t0 * kv_tok), nt * kv_tok, cudaMemcpyHostToDevice,
+                            hp.h2d);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(hp.in[c], hp.h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in[c], 0);
+    if (e != cudaSuccess) break;
+    if (int rc = varlen_impl(q_dev, k_dev, v_dev, o_dev, lse_dev, cu_seqlens_dev + a, cu_seqlens_dev + a,
+                             cu_seqlens_host + a, cu_seqlens_host + a, b - a, len_max, len_max, total_tokens,
+                             total_tokens, Hq, Hkv, D, dtype, st, causal, -1, -1, scale, stream, true, nullptr, 0,
+                             true, ks))
+      return rc;
+    e = cudaEventRecord(hp.out[c], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.out[c], 0);
+    if (e == cudaSuccess && nt > 0)
+      e = cudaMemcpyAsync(atw(o_host, t0 * q_tok), at(o_dev, t0 * q_tok), nt * q_tok, cudaMemcpyDeviceToHost, hp.d2h);
+    if (e == cudaSuccess && nt > 0 && lse_host)
+      e = cudaMemcpy2DAsync(lse_host + t0, (size_t)T * sizeof(float), lse_dev + t0, (size_t)T * sizeof(float),
+                            (size_t)nt * sizeof(float), (size_t)Hq, cudaMemcpyDeviceToHost, hp.d2h);
+  }
+  if (e == cudaSuccess) e = pipe_end(hp, s);
   if (e != cudaSuccess) return fail_cuda(e);
   return ETATTN_OK;
 }

@@ -337,11 +337,19 @@ int attn_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, flo
  *   *_dev : caller-owned DEVICE buffers of the same sizes and layouts; the
  *           inputs are staged there and the outputs computed there.  lse_dev
  *           must be NULL exactly when lse_host is NULL.
- * On `stream` the call enqueues: three host-to-device copies, the attention
- * kernel, and the device-to-host copies of O and lse.  It returns once they
- * are enqueued; synchronise `stream` before reading o_host / lse_host.
- * Arguments are validated (as for attn_fwd, on the device buffers) before
- * anything is enqueued.  Nothing is allocated.
+ * The call cuts the problem into up to 8 chunks (runs of whole batches; with
+ * B = 1, runs of KV heads with their query heads) and pipelines them: chunk
+ * c + 1's inputs are copied to the device while chunk c's kernel runs, and
+ * chunk c's outputs are copied back meanwhile.  The kernels run on `stream`;
+ * the copies run on two copy streams of the library's own (one per device,
+ * created on first use and kept), which first wait for the work already on
+ * `stream`, and `stream` waits for the last copy before anything enqueued
+ * after the call.  So, seen from `stream`, the call is ordered like one
+ * operation: synchronise `stream` before reading o_host / lse_host, and do
+ * not change q_host / k_host / v_host before then.  It returns once all of
+ * it is enqueued.  Arguments are validated (as for attn_fwd, on the device
+ * buffers) before anything is enqueued.  Each chunk computes its rows as
+ * the whole call would.  Nothing is allocated on the device.
  */
 int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
                   void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int B, int Hq, int Hkv, int N,
@@ -352,11 +360,29 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
  *   q/k/v/o host and device buffers: contiguous [T,H,D]; lse [Hq,T] FP32 or NULL.
  *   cu_seqlens_host (required) is validated on the host and copied to the
  *   caller-owned device buffer cu_seqlens_dev (int32 [num_seqs+1]).
+ * The chunks are the runs of whole sequences that attn_fwd_varlen_host_plan
+ * returns for max_chunks = 8 (about equal token counts): a chunk's tokens are
+ * contiguous rows of q/k/v/o and one column band of lse.
  */
 int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
                          const int32_t* cu_seqlens_host, void* q_dev, void* k_dev, void* v_dev, void* o_dev,
                          float* lse_dev, int32_t* cu_seqlens_dev, int num_seqs, int max_seqlen, int total_tokens,
                          int Hq, int Hkv, int D, int dtype, int causal, float scale, void* stream);
+
+/*
+ * attn_fwd_varlen_host_plan: the chunks attn_fwd_varlen_host pipelines.
+ * Host-only (no device call).  Cuts the num_seqs sequences of the HOST
+ * offsets cu_seqlens_host[0..num_seqs] into k <= min(max_chunks, 8, num_seqs)
+ * runs of consecutive sequences of about equal token counts: a run ends after
+ * the first sequence whose cumulative token count reaches the next multiple
+ * of total / k_max (the last run takes the rest).  seq_bounds (caller-owned,
+ * int32 [k + 1], so 9 entries suffice) receives 0 = b_0 < b_1 < ... < b_k =
+ * num_seqs; run c holds sequences b_c .. b_(c+1) - 1.  Returns k (0 when
+ * num_seqs == 0), or a negative status: -ETATTN_ERR_NULL_PTR,
+ * -ETATTN_ERR_BAD_SHAPE (num_seqs < 0 or max_chunks < 1),
+ * -ETATTN_ERR_BAD_SEQLENS (offsets that decrease).
+ */
+int attn_fwd_varlen_host_plan(const int32_t* cu_seqlens_host, int num_seqs, int max_chunks, int32_t* seq_bounds);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* etattn_status_string(int code);

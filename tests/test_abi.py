@@ -428,3 +428,65 @@ def test_wait_selftest_checks_its_limit_before_any_device_work():
     assert B.etattn_selftest_wait_timeout(1000) == (12 if not torch.cuda.is_available() else 0)
     if torch.cuda.is_available():
         B.etattn_read_device_status(clear=True)
+
+
+# ---------------------------------------------------------------- host-buffer chunk plan
+
+def _check_plan(lengths, max_chunks):
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    k, b = B.attn_fwd_varlen_host_plan(cu, max_chunks)
+    n = len(lengths)
+    if n == 0:
+        assert k == 0 and b == []
+        return k, b
+    k_max = max(1, min(max_chunks, 8, n))
+    assert 1 <= k <= k_max and len(b) == k + 1
+    assert b[0] == 0 and b[-1] == n and all(x < y for x, y in zip(b, b[1:]))
+    T = cu[-1]
+    if T > 0:
+        for c in range(k - 1):  # run c (all but the last) ends at its first sequence reaching its share
+            share = (c + 1) * T
+            assert cu[b[c + 1]] * k_max >= share
+            assert b[c + 1] - 1 == b[c] or cu[b[c + 1] - 1] * k_max < share
+    return k, b
+
+
+def test_host_plan_packed_workload_runs():
+    # the packed benchmark batch's 16 lengths: runs of about T / 8 tokens, cut by hand
+    lengths = [12464, 9413, 538, 10743, 5700, 4308, 920, 13928, 1373, 11450, 7567, 2584, 11849, 4442, 12655, 14891]
+    k, b = _check_plan(lengths, 8)
+    assert k == 8 and b == [0, 2, 4, 8, 10, 11, 14, 15, 16]
+
+
+@pytest.mark.parametrize("lengths,max_chunks,want", [
+    ([100] * 16, 8, [0, 2, 4, 6, 8, 10, 12, 14, 16]),      # equal lengths: equal runs
+    ([100] * 16, 99, [0, 2, 4, 6, 8, 10, 12, 14, 16]),     # at most 8 runs
+    ([100] * 3, 8, [0, 1, 2, 3]),                          # at most one run per sequence
+    ([100] * 4, 1, [0, 4]),                                # one run: the whole batch
+    ([10000, 1, 1, 1], 8, [0, 1, 2, 3, 4]),
+    ([1, 1, 1, 10000], 8, [0, 4]),                         # the long last sequence holds every share
+    ([0, 0, 0], 8, [0, 3]),                                # no tokens: one run
+    ([5, 0, 7, 0, 3], 2, [0, 3, 5]),
+])
+def test_host_plan_examples(lengths, max_chunks, want):
+    k, b = _check_plan(lengths, max_chunks)
+    assert b == want
+
+
+def test_host_plan_random_properties():
+    import random
+    rng = random.Random(3)
+    for _ in range(300):
+        n = rng.randint(0, 40)
+        lengths = [rng.choice([0, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(n)]
+        _check_plan(lengths, rng.randint(1, 12))
+
+
+def test_host_plan_rejects_bad_arguments():
+    assert B.attn_fwd_varlen_host_plan([0, 5, 3], 8)[0] == -9     # offsets decrease
+    assert B.attn_fwd_varlen_host_plan([0, 5], 0)[0] == -3        # max_chunks < 1
+    assert B.attn_fwd_varlen_host_plan([], 8)[0] == -3            # num_seqs = -1
+    lib = B.load_library()
+    assert lib.attn_fwd_varlen_host_plan(None, 1, 8, (ctypes.c_int32 * 9)()) == -1

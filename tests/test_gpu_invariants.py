@@ -207,6 +207,91 @@ def test_host_buffer_entry_points_match_device_path():
     assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
 
 
+def _host_batched(inp, causal, s):
+    pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+    Bn, Hq, N, D = inp["q"].shape
+    Hkv = inp["k"].shape[1]
+    dq, dk, dv = (torch.empty_like(pin[n], device="cuda") for n in ("q", "k", "v"))
+    do = torch.empty(pin["q"].shape, dtype=pin["q"].dtype, device="cuda")
+    dl = torch.empty((Bn, Hq, N), dtype=torch.float32, device="cuda")
+    oh = torch.empty(pin["q"].shape, dtype=pin["q"].dtype).pin_memory()
+    lh = torch.empty((Bn, Hq, N), dtype=torch.float32).pin_memory()
+    dt = 1 if pin["q"].dtype == torch.bfloat16 else 0
+    rc = binding.attn_fwd_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(), oh.data_ptr(),
+                               lh.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(),
+                               dl.data_ptr(), Bn, Hq, Hkv, N, D, dt, int(causal), 1 / D ** 0.5, s.cuda_stream)
+    assert rc == 0
+    return oh, lh, (pin, dq, dk, dv, do, dl)
+
+
+@pytest.mark.parametrize("shape", [(3, 8, 4, 700, 128), (1, 8, 4, 900, 128), (1, 6, 6, 260, 64), (5, 4, 1, 129, 32)])
+def test_host_pipeline_batched_chunks_match_device_path(shape):
+    """attn_fwd_host pipelines runs of batches (or, with one batch, of KV
+    heads); every chunk's rows equal the device-resident call bit for bit."""
+    Bn, Hq, Hkv, N, D = shape
+    s = torch.cuda.Stream()
+    for causal in (True, False):
+        inp = W.random_qkv(Bn, Hq, Hkv, N, D, torch.bfloat16, seed=40 + Bn + N)
+        o_ref, l_ref = run_gpu(inp, causal)
+        oh, lh, _ = _host_batched(inp, causal, s)
+        s.synchronize()
+        assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+
+
+def test_host_pipeline_packed_chunks_match_device_path():
+    """attn_fwd_varlen_host over many sequences (several chunks, empty and
+    one-token sequences among them) equals the device-resident call bit for
+    bit, and the plan it follows has several runs."""
+    lengths = [300, 0, 1, 1200, 77, 640, 0, 2049, 129, 513, 900, 5, 1500, 256]
+    for dt, D in ((torch.bfloat16, 128), (torch.float16, 64)):
+        inp = W.random_varlen(lengths, 4, 2, D, dt, seed=41)
+        cu_h = inp["cu_seqlens"].pin_memory()
+        assert binding.attn_fwd_varlen_host_plan(cu_h.tolist())[0] >= 4
+        for causal in (True, False):
+            o_ref, l_ref = run_gpu(inp, causal)
+            T = sum(lengths)
+            s = torch.cuda.Stream()
+            pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+            dq, dk, dv = (torch.empty_like(pin[n], device="cuda") for n in ("q", "k", "v"))
+            do, dl = torch.empty_like(o_ref), torch.empty_like(l_ref)
+            cu_d = torch.empty(len(lengths) + 1, dtype=torch.int32, device="cuda")
+            oh = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+            lh = torch.empty(l_ref.shape, dtype=torch.float32).pin_memory()
+            rc = binding.attn_fwd_varlen_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
+                                              oh.data_ptr(), lh.data_ptr(), cu_h.data_ptr(), dq.data_ptr(),
+                                              dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dl.data_ptr(),
+                                              cu_d.data_ptr(), len(lengths), max(lengths), T, 4, 2, D,
+                                              1 if dt == torch.bfloat16 else 0, int(causal), 1 / D ** 0.5,
+                                              s.cuda_stream)
+            assert rc == 0
+            s.synchronize()
+            assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+
+
+def test_host_pipeline_back_to_back_calls_are_ordered():
+    """Two host-buffer calls enqueued back to back on one stream, the second
+    reusing the first one's device buffers with other inputs: each result is
+    that of its own inputs (the second call's uploads wait for the first call's
+    kernels and downloads)."""
+    s = torch.cuda.Stream()
+    a = W.random_qkv(4, 8, 2, 1024, 128, torch.bfloat16, seed=42)
+    b = W.random_qkv(4, 8, 2, 1024, 128, torch.bfloat16, seed=43)
+    oa_ref, la_ref = run_gpu(a, True)
+    ob_ref, lb_ref = run_gpu(b, True)
+    oh_a, lh_a, bufs = _host_batched(a, True, s)
+    pin, dq, dk, dv, do, dl = bufs
+    pin_b = {n: b[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+    oh_b = torch.empty_like(oh_a).pin_memory()
+    lh_b = torch.empty_like(lh_a).pin_memory()
+    rc = binding.attn_fwd_host(pin_b["q"].data_ptr(), pin_b["k"].data_ptr(), pin_b["v"].data_ptr(), oh_b.data_ptr(),
+                               lh_b.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(),
+                               dl.data_ptr(), 4, 8, 2, 1024, 128, 1, 1, 1 / 128 ** 0.5, s.cuda_stream)
+    assert rc == 0
+    s.synchronize()
+    assert torch.equal(oh_a, oa_ref.cpu()) and torch.equal(lh_a, la_ref.cpu())
+    assert torch.equal(oh_b, ob_ref.cpu()) and torch.equal(lh_b, lb_ref.cpu())
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_repeated_calls_bit_identical_many_ctas(causal):
     """Many CTAs, repeated calls on the same inputs: results are bit-identical
