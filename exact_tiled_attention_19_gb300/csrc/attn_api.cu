@@ -1240,6 +1240,31 @@ int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_h
   for (int i = 0; i <= num_seqs; ++i) pre[i] = cu_seqlens_host[i];
   int32_t bounds[kHostChunks + 1];
   const int k = plan_runs(pre.data(), num_seqs, kHostChunks, bounds);
+  // Processing order: nothing overlaps the first run's upload, nor the last
+  // run's kernel and download, so the run with the fewest tokens goes first
+  // and, of the others, the one with the least causal work (sum of squared
+  // lengths) last; the rest keep their order.
+  int order[kHostChunks];
+  {
+    int first = 0, last = -1;
+    for (int c = 1; c < k; ++c)
+      if (pre[bounds[c + 1]] - pre[bounds[c]] < pre[bounds[first + 1]] - pre[bounds[first]]) first = c;
+    double best = 0.0;
+    for (int c = 0; c < k; ++c) {
+      if (c == first) continue;
+      double work = 0.0;
+      for (int i = bounds[c]; i < bounds[c + 1]; ++i) work += (double)(pre[i + 1] - pre[i]) * (pre[i + 1] - pre[i]);
+      if (last < 0 || work < best) {
+        last = c;
+        best = work;
+      }
+    }
+    int n = 0;
+    order[n++] = first;
+    for (int c = 0; c < k; ++c)
+      if (c != first && c != last) order[n++] = c;
+    if (last >= 0) order[n++] = last;
+  }
   int dev = 0, num_sms = 0;
   int* status = nullptr;
   if (int rc = current_device(&dev, &status, &num_sms)) return rc;
@@ -1255,7 +1280,7 @@ int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_h
     e = cudaMemcpyAsync(cu_seqlens_dev, cu_seqlens_host, (size_t)(num_seqs + 1) * sizeof(int32_t),
                         cudaMemcpyHostToDevice, hp.h2d);
   for (int c = 0; c < k && e == cudaSuccess; ++c) {
-    const int a = bounds[c], b = bounds[c + 1];
+    const int a = bounds[order[c]], b = bounds[order[c] + 1];
     const int64_t t0 = cu_seqlens_host[a], nt = (int64_t)cu_seqlens_host[b] - t0;
     int len_max = 0;
     for (int i = a; i < b; ++i) len_max = std::max(len_max, cu_seqlens_host[i + 1] - cu_seqlens_host[i]);

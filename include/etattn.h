@@ -362,7 +362,9 @@ int attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, vo
  *   caller-owned device buffer cu_seqlens_dev (int32 [num_seqs+1]).
  * The chunks are the runs of whole sequences that attn_fwd_varlen_host_plan
  * returns for max_chunks = 8 (about equal token counts): a chunk's tokens are
- * contiguous rows of q/k/v/o and one column band of lse.
+ * contiguous rows of q/k/v/o and one column band of lse.  The run with the
+ * fewest tokens is processed first and, of the others, the one whose lengths
+ * have the smallest sum of squares last; the rest in order.
  */
 int attn_fwd_varlen_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
                          const int32_t* cu_seqlens_host, void* q_dev, void* k_dev, void* v_dev, void* o_dev,
