@@ -268,6 +268,41 @@ def test_host_pipeline_packed_chunks_match_device_path():
             assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
 
 
+@pytest.mark.parametrize("layout", ["batched", "packed"])
+def test_host_pipeline_without_lse_and_small_heads(layout):
+    """The pipelined host calls with lse omitted (no lse download; lse_dev NULL
+    too), D = 32 and FP16: O equals the device-resident call bit for bit."""
+    s = torch.cuda.Stream()
+    if layout == "batched":
+        inp = W.random_qkv(3, 4, 2, 333, 32, torch.float16, seed=44)
+        o_ref, _ = run_gpu(inp, True)
+        pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+        dq, dk, dv = (torch.empty_like(pin[n], device="cuda") for n in ("q", "k", "v"))
+        do = torch.empty_like(o_ref)
+        oh = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+        rc = binding.attn_fwd_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(), oh.data_ptr(), 0,
+                                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), 0, 3, 4, 2, 333, 32,
+                                   0, 1, 1 / 32 ** 0.5, s.cuda_stream)
+    else:
+        lengths = [513, 7, 0, 260, 1025, 64, 300, 129, 900]
+        inp = W.random_varlen(lengths, 4, 2, 32, torch.float16, seed=45)
+        o_ref, _ = run_gpu(inp, True)
+        T = sum(lengths)
+        pin = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v")}
+        cu_h = inp["cu_seqlens"].pin_memory()
+        dq, dk, dv = (torch.empty_like(pin[n], device="cuda") for n in ("q", "k", "v"))
+        do = torch.empty_like(o_ref)
+        cu_d = torch.empty(len(lengths) + 1, dtype=torch.int32, device="cuda")
+        oh = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+        rc = binding.attn_fwd_varlen_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
+                                          oh.data_ptr(), 0, cu_h.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                          dv.data_ptr(), do.data_ptr(), 0, cu_d.data_ptr(), len(lengths),
+                                          max(lengths), T, 4, 2, 32, 0, 1, 1 / 32 ** 0.5, s.cuda_stream)
+    assert rc == 0
+    s.synchronize()
+    assert torch.equal(oh, o_ref.cpu())
+
+
 def test_host_pipeline_back_to_back_calls_are_ordered():
     """Two host-buffer calls enqueued back to back on one stream, the second
     reusing the first one's device buffers with other inputs: each result is
