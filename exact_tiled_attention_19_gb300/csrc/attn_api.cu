@@ -272,10 +272,19 @@ cudaError_t launch(int D, int dtype, const CUtensorMap& q, const CUtensorMap& k,
   const bool bf = dtype == ETATTN_BF16;
   const int64_t splits = p.part_o != nullptr ? p.num_splits : 1;
   const int64_t blocks1 = (tokens + 127) / 128, blocks2 = (tokens + 255) / 256;
-  // ks_force >= 0: a chunk of a larger call takes the whole call's key-split
-  // choice (the split changes the order of the sum over key tiles).
+  // The key split halves every CTA's key range and doubles the CTAs: for
+  // problems that would not fill half the SMs, and for general (unequal-
+  // length) problems of at least 16 key tiles whose equal CTAs would leave the
+  // last wave partly empty: c CTAs take ceil(c / SMs) waves of one length, 2c
+  // key-split CTAs ceil(2c / SMs) waves of half of it (taken when that is at
+  // least 5 % shorter).  ks_force >= 0: a chunk of a larger call takes the
+  // whole call's choice (the split changes the order of the sum over key
+  // tiles).
+  const int64_t ctas2 = blocks2 * (int64_t)gy * gz, ctas1 = blocks1 * (int64_t)gy * gz;
+  const bool ks_waves = general && key_tiles >= 16 && ctas2 > num_sms &&
+                        ((ctas1 + num_sms - 1) / num_sms) * 100 < ((ctas2 + num_sms - 1) / num_sms) * 2 * 95;
   const bool ksplit = splits == 1 && p.qpack == 1 && p.num_global == 0 && key_tiles >= 2 &&
-                      (ks_force >= 0 ? ks_force == 1 : 2 * blocks1 * (int64_t)gy * gz <= num_sms);
+                      (ks_force >= 0 ? ks_force == 1 : (2 * ctas1 <= num_sms || ks_waves));
   // Up to 128 query rows fill one sub-tile: a second one would only idle.
   const int nsub = (p.qpack > 1 || tokens <= 128 || blocks2 * (int64_t)gy * gz * splits < num_sms) ? 1 : 2;
   const int64_t gx = (ksplit || nsub == 1 ? blocks1 : blocks2) * splits;
