@@ -653,7 +653,6 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   int* status = nullptr;
   int num_sms = 0;
   if (int rc = current_device(&dev, &status, &num_sms)) return rc;
-  (void)num_sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = dtype == ETATTN_BF16;
   const int nq_pad = (Nq + 127) / 128 * 128;
@@ -722,7 +721,22 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = status;
     p.hn_swapped = (swq ? 1 : 0) | (swk ? 2 : 0) | (swv ? 4 : 0) | (swd ? 8 : 0);
-    const dim3 grid((unsigned)((Nk + 127) / 128), (unsigned)Hkv, (unsigned)B);
+    // Grouped longest-first order (the kernel's bwd_cta_coords), as for the
+    // forward launch: groups of G (KV head, batch) pairs, G the smallest power
+    // of two whose CTAs fill the SMs once.
+    const int64_t gx = (Nk + 127) / 128, pairs = (int64_t)Hkv * B;
+    dim3 grid((unsigned)gx, (unsigned)Hkv, (unsigned)B);
+    p.grid_x = (int)gx;
+    p.grid_y = Hkv;
+    p.sched_q = p.sched_rem = 0;
+    if (gx * pairs > num_sms && gx * pairs <= 0x7fffffffLL) {
+      int64_t G = 1;
+      while (G * gx < num_sms && G < pairs) G *= 2;
+      const int64_t groups = (pairs + G - 1) / G;
+      p.sched_q = (int)(pairs / groups);
+      p.sched_rem = (int)(pairs % groups);
+      grid = dim3((unsigned)(gx * pairs), 1, 1);
+    }
     cudaError_t e;
     switch (D) {
       case 32:

@@ -70,7 +70,33 @@ struct BwdParams {
   float scale, scale_log2;
   int* status;
   int hn_swapped;                // bit 0/1/2/3: the q/k/v/dO tensor map orders (d, head, token, batch)
+  int grid_x, grid_y;            // key blocks, KV heads (the logical grid's x and y extents)
+  int sched_q, sched_rem;        // > 0: 1-D launch in grouped longest-first order (bwd_cta_coords)
 };
+
+// The logical (key block, KV head, batch) of this CTA.  With sched_q > 0 the
+// grid is launched 1-D and the (KV head, batch) pairs (head fastest) are cut
+// into contiguous groups of near-equal size (sched_rem groups of sched_q + 1
+// pairs, then groups of sched_q); a group's CTAs come one after another,
+// ordered by key block and then by pair.  Key block 0 is read by the most
+// query blocks, so every group's longest CTAs start first and the last CTAs
+// to start are the shortest ones of the last group, while the CTAs running at
+// any time read the Q, dO and dQ rows of one group.  (Plain divisions: a
+// backward CTA runs for many steps, and the map is a few hundred cycles.)
+__device__ __forceinline__ int3 bwd_cta_coords(const BwdParams& p) {
+  if (p.sched_q <= 0) return make_int3((int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z);
+  const uint32_t lin = blockIdx.x, gx = (uint32_t)p.grid_x, gy = (uint32_t)p.grid_y;
+  const uint32_t q = (uint32_t)p.sched_q, big = (uint32_t)p.sched_rem * (q + 1);  // pairs in the larger groups
+  const uint32_t pi = lin / gx;  // CTA lin lies in the group holding the pi-th pair
+  const bool large = pi < big;
+  const uint32_t size = large ? q + 1 : q;
+  const uint32_t first = large ? pi / size * size : big + (pi - big) / q * q;
+  const uint32_t r = lin - first * gx;
+  const uint32_t x = r / size;
+  const uint32_t pair = first + (r - x * size);
+  const uint32_t z = pair / gy;
+  return make_int3((int)x, (int)(pair - z * gy), (int)z);
+}
 
 template <int D>
 struct BwdCfg {
@@ -495,7 +521,7 @@ __device__ __forceinline__ void bwd_dq(BwdBarriers& sb, uint8_t* smem, uint32_t 
   if (lane == 0) bulk_wait_all();
 }
 
-// Grid: x = key block, y = key/value head, z = batch.
+// Logical grid: x = key block, y = key/value head, z = batch (bwd_cta_coords).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(512, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -507,9 +533,10 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   BwdUnit u;
-  u.kb0 = blockIdx.x * C::BN;
-  u.hk = blockIdx.y;
-  u.b = blockIdx.z;
+  const int3 cta = bwd_cta_coords(p);
+  u.kb0 = cta.x * C::BN;
+  u.hk = cta.y;
+  u.b = cta.z;
   u.h0 = u.hk * p.group;
   {
     // Query rows that can read one of the keys kb0 .. kb0 + 127 (clipped to Nk).

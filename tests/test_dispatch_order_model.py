@@ -9,7 +9,10 @@ every CTA of a larger x (a shorter causal block) starts after every CTA of a
 smaller x; groups are contiguous ranges of (y, z) pairs of near-equal size.
 A list-scheduling model of the GPU (one CTA per SM, each SM taking the next
 CTA in launch order) shows the grouped order removing the causal tail of the
-plain 3-D order on the batched and packed workloads."""
+plain 3-D order on the batched and packed workloads.  The backward launch
+(attn_bwd_kernel.cuh, bwd_cta_coords) uses the same map with x the key block
+(block 0, read by every query block, is the longest); the model shows the same
+for its CTAs, whose lengths are the query steps they walk."""
 
 import heapq
 
@@ -135,3 +138,26 @@ def test_multiply_shift_division_is_exact_below_2_31(d):
     for n in ns:
         if 0 <= n < 2 ** 31:
             assert (n * m) >> k == n // d, (n, d)
+
+
+def _backward_ctas(B, Hq, Hkv, N, order):
+    """(launch order) per-CTA step counts of the causal backward launch: key
+    block kb walks the query blocks kb .. N/128 - 1 of each of the group's
+    Hq / Hkv query heads."""
+    gx, gy, gz = (N + 127) // 128, Hkv, B
+
+    def work(x, y, z):
+        return (gx - x) * (Hq // Hkv)
+
+    if order == "grid":
+        return [work(x, y, z) for z in range(gz) for y in range(gy) for x in range(gx)]
+    q, rem = group_sizes(gx, gy, gz)
+    return [work(*cta_coords(lin, gx, gy, gz, q, rem)[:3]) for lin in range(gx * gy * gz)]
+
+
+@pytest.mark.parametrize("shape,gain", [((4, 16, 16, 4096), 0.02), ((2, 32, 8, 8192), 0.05)])
+def test_grouped_order_shortens_the_backward_tail(shape, gain):
+    grid, grouped = _makespan(_backward_ctas(*shape, "grid")), _makespan(_backward_ctas(*shape, "grouped"))
+    ideal = sum(2.0 + n for n in _backward_ctas(*shape, "grid")) / SMS
+    assert grouped <= grid * (1 - gain)
+    assert grouped <= ideal * 1.05
