@@ -184,3 +184,14 @@ def test_gqa_packing_packed_batch():
     inp = W.random_varlen(lq, 8, 2, 128, torch.bfloat16, seed=29, lengths_k=lk)
     o, lse = run_gpu(inp, True)
     compare_full(inp, o, lse, True, default_scale(128), torch.bfloat16)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_key_split_wave_model_launch_full(causal):
+    """A general (Lq != Lk) launch whose 192 equal two-sub-tile CTAs would
+    leave its second wave mostly empty on a 148- or 152-SM GPU, with 32 key
+    tiles per query block: the launcher takes the key split (384 CTAs of half
+    the keys each).  Every element against the oracle, at the stated bounds."""
+    inp = W.random_qkv(1, 24, 6, 2048, 128, torch.bfloat16, seed=61, Nk=4096)
+    o, lse = run_gpu(inp, causal)
+    compare_full(inp, o, lse, causal, default_scale(128), torch.bfloat16)
