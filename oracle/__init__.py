@@ -38,7 +38,7 @@ force; none is "parity unpinned".
 
 from .dense import attention_dense, attention_varlen, attention_rows, attention_varlen_rows
 from .online_state import State, empty_state, state_of_block, merge, finalize
-from .backward import attention_backward_dense, attention_backward_sampled, backward_magnitudes
+from .backward import attention_backward_dense, attention_backward_sampled, backward_d_rounding, backward_magnitudes
 
 __all__ = [
     "attention_dense",
@@ -52,5 +52,6 @@ __all__ = [
     "finalize",
     "attention_backward_dense",
     "attention_backward_sampled",
+    "backward_d_rounding",
     "backward_magnitudes",
 ]

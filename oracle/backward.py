@@ -135,6 +135,40 @@ def attention_backward_sampled(q, k, v, do, q_rows, k_rows, *, causal, scale, gr
     return dq, dk, dv
 
 
+def _d_magnitude(p, do_rows, v):
+    """|D|_i = sum_d |dO_id| sum_l P_il |v_ld|: the absolute terms of
+    D_i = <dO_i, O_i> with O_i = sum_l P_il v_l."""
+    return np.sum(p * (np.abs(do_rows) @ np.abs(v).T), axis=1)
+
+
+def backward_d_rounding(q, k, v, do, *, causal, scale, window_left=-1, window_right=-1):
+    """How far an error of relative size 1 in each O element moves the
+    gradients when D is taken as D_i = <dO_i, O_i> from the stored output
+    (lesson 03's saved normalisation state), not a result the kernel computes.
+    Rounding every O element to a 16-bit type (relative error at most u)
+    moves D_i by at most u |D|_i, |D|_i = sum_d |dO_id| sum_l P_il |v_ld|;
+    through dS_ij = P_ij (dP_ij - D_i) that moves
+      dQ_i by at most u E_dQ_i,  E_dQ_i = scale * |D|_i sum_j P_ij |k_j|
+      dK_j by at most u E_dK_j,  E_dK_j = scale * sum_i P_ij |D|_i |q_i|
+    and dV not at all.  Returns (E_dQ, E_dK), shaped as dQ and dK (dK terms
+    summed over the group)."""
+    q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
+    B, Hq, Nq, D = q.shape
+    group = Hq // k.shape[1]
+    eq = np.zeros_like(q)
+    ek = np.zeros_like(k)
+    for b in range(B):
+        for h in range(Hq):
+            hk = kv_head_of(h, group)
+            for r0 in range(0, Nq, _ROW_CHUNK):
+                rows = np.arange(r0, min(Nq, r0 + _ROW_CHUNK))
+                p = _probabilities(q[b, h, rows], rows, k[b, hk], causal, scale, Nq, window_left, window_right)
+                pd = p * _d_magnitude(p, do[b, h, rows], v[b, hk])[:, None]
+                eq[b, h, rows] = scale * (pd @ np.abs(k[b, hk]))
+                ek[b, hk] += scale * (pd.T @ np.abs(q[b, h, rows]))
+    return eq, ek
+
+
 def backward_magnitudes(q, k, v, do, *, causal, scale, window_left=-1, window_right=-1):
     """Sums of the absolute values of the terms of each gradient element, the
     scale against which rounding errors in a 16-bit implementation are

@@ -172,24 +172,27 @@ def default_scale(D):
 def compare_backward(inputs, dout, grads, causal, scale, dtype, window_left=-1, window_right=-1):
     """Compare dQ, dK, dV element by element with the FP64 oracle.  Bound
     derived from the arithmetic (u the input type's relative half-ulp): the
-    kernel rounds P and dS to the input type (relative u each), takes
-    D = <dO, O> from the forward's rounded O, accumulates in FP32 and rounds
-    each gradient once; every term of an element therefore moves by a few u
-    of its magnitude, so |dG| <= u |G| + 8 u M + a floor of 1e-6 max M, with M
-    the sum of the absolute values of the element's terms
-    (oracle.backward_magnitudes).  Returns the worst error / bound ratio."""
+    kernel rounds P and dS to the input type (relative u each), accumulates
+    in FP32 and rounds each gradient once, so every term of an element moves
+    by a few u of its magnitude: u |G| + 8 u M, with M the sum of the
+    absolute values of the element's terms (oracle.backward_magnitudes).  It
+    also takes D = <dO, O> from the forward's O rounded to the input type,
+    which moves dQ and dK by at most u E (oracle.backward_d_rounding; E grows
+    with the cancellation in dP = <dO, v>, which M does not see); plus a
+    floor of 1e-6 max M.  Returns the worst error / bound ratio."""
     q64, k64, v64, do64 = to64(inputs["q"]), to64(inputs["k"]), to64(inputs["v"]), to64(dout)
     kw = dict(causal=causal, scale=scale, window_left=window_left, window_right=window_right)
     refs = oracle.attention_backward_dense(q64, k64, v64, do64, **kw)
     mags = oracle.backward_magnitudes(q64, k64, v64, do64, **kw)
+    eq, ek = oracle.backward_d_rounding(q64, k64, v64, do64, **kw)
     u = HALF_ULP[dtype]
     worst = 0.0
-    for name, g, r, m in zip(("dq", "dk", "dv"), grads, refs, mags):
+    for name, g, r, m, e in zip(("dq", "dk", "dv"), grads, refs, mags, (eq, ek, 0.0)):
         g64 = to64(g)
         assert np.all(np.isfinite(g64)), f"non-finite {name}"
         if r.size == 0:
             continue
-        bound = u * np.abs(r) + 8 * u * m + 1e-6 * max(float(m.max()), 1e-30)
+        bound = u * np.abs(r) + 8 * u * m + u * e + 1e-6 * max(float(m.max()), 1e-30)
         ratio = float((np.abs(g64 - r) / bound).max())
         assert ratio <= 1.0, f"{name}: error {float(np.abs(g64 - r).max()):.3g} exceeds the bound ({ratio:.2f}x)"
         worst = max(worst, ratio)

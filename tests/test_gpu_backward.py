@@ -57,6 +57,16 @@ def test_gqa_multihead(layout):
     compare_backward(inp, dout, grads, True, default_scale(128), torch.bfloat16)
 
 
+def test_uneven_dispatch_groups():
+    """41 (KV head, batch) pairs of 8 key blocks: the grouped longest-first
+    launch cuts them into groups of 21 and 20 pairs (the remainder path of
+    the 1-D order); every gradient element against the oracle."""
+    inp = W.random_qkv(1, 41, 41, 1024, 64, torch.float16, seed=71)
+    dout = dout_like(inp["q"], 72)
+    grads = fwd_bwd(inp, dout, True)
+    compare_backward(inp, dout, grads, True, default_scale(64), torch.float16)
+
+
 @pytest.mark.parametrize("Nq,Nk", [(100, 700), (700, 100), (1, 300), (300, 1)])
 def test_unequal_lengths(Nq, Nk):
     inp = W.random_qkv(1, 4, 2, Nq, 64, torch.bfloat16, seed=Nq + Nk, Nk=Nk)
